@@ -1,0 +1,477 @@
+"""Plain CPU oracle for group-wise low-bit KV-cache quantization and
+single-token decode attention over the quantized cache.
+
+TEST INFRASTRUCTURE. This module is the checker, not the product: only
+``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` /
+``--impl reference`` legs of ``bench.py`` may import it. The CUDA library
+never calls it, and it shares no code, constant table or helper with the
+CUDA path.
+
+What it computes, and where the pages fix it. Pages are cited by a short
+name, their address and the section on the page:
+
+* [TurboQuant-3bit] "TurboQuant 3-bit KV-cache quantization",
+  dpshk.com/news/6341316
+* [KVQuant] "KVQuant: breaking the KV-cache memory wall",
+  cf-1.com/news/2306543
+* [TurboQuant-mem] "TurboQuant: the KV cache as memory killer",
+  demingchina.com/news/57821
+* [W4A8-FA3] "W8A8/W4A8, sparsity, FlashAttention-3 and KV-cache
+  quantization in practice", discosf.com/news/4854722
+* [NIAH-q8_0] "TurboQuant NIAH single-needle q8_0 KV-cache measurements",
+  cf-1.com/news/5482713
+
+Precision. The codec decides integer codes, so it runs in fp32 with IEEE
+round-to-nearest-even at every step (numpy float32 ufuncs do not contract
+to FMA): a code is an integer decided by floating point, and both sides take
+that decision in the same precision. Dequantization and attention run in
+fp64. Readings of points the pages leave open are listed in the design doc
+(readings R1..R12) and restated where they are used.
+
+Every function here is pinned by ``tests/test_oracle_pins.py`` against
+values the pages print, closed forms, brute force or library routines.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+
+SYM_PER_TOKEN = 0
+ASYM_PER_TOKEN = 1
+ASYM_PER_CHANNEL = 2
+
+
+# ---------------------------------------------------------------------------
+# Footprint
+# ---------------------------------------------------------------------------
+
+def fp16_kv_cache_bytes(num_layers, num_kv_heads, head_dim, seq_len,
+                        bytes_per_elem=2, batch=1):
+    """Unquantized KV-cache size: K and V (factor 2) for every layer, KV head,
+    channel and cached token.
+
+    [TurboQuant-3bit] §2.1 gives the per-token form 2 x L x d_head x h x bytes;
+    [TurboQuant-mem] §1.2 gives the element count 2 x L x H x D x S.
+    """
+    return 2 * num_layers * num_kv_heads * head_dim * seq_len * bytes_per_elem * batch
+
+
+def codes_per_word(bits):
+    """Codes held by one 32-bit word: 32/b for b in {4, 8}; for b = 3 the
+    word holds ten codes and its top two bits stay zero (the 3-bit layout
+    of ten codes per word with two spare bits)."""
+    if bits == 3:
+        return 10
+    if bits in (4, 8):
+        return 32 // bits
+    raise ValueError("bits must be 3, 4 or 8")
+
+
+def words_per_row(bits, head_dim):
+    return -(-head_dim // codes_per_word(bits))
+
+
+def packed_cache_bytes(num_layers, batch, num_kv_heads, head_dim, seq_len,
+                       k_bits, v_bits, k_mode, v_mode, k_group, v_group,
+                       outliers_per_row=0):
+    """Algorithmic bytes of a quantized cache holding ``seq_len`` tokens per
+    layer: packed codes + fp16 metadata + CSR outliers (int32 row pointers,
+    uint16 columns, fp16 values). Keys in per-channel mode hold floor(S/T)
+    quantized blocks plus an fp16 residual of S mod T keys (reading R7).
+
+    Metadata per group: an fp16 scale for symmetric groups (zero point 0,
+    [NIAH-q8_0] §1.2); an fp16 scale and an fp16 zero point for asymmetric
+    groups ([TurboQuant-3bit] §3.1, [W4A8-FA3] §2.4).
+    """
+    streams = num_layers * batch * num_kv_heads
+    total = 0
+    for bits, mode, group, is_k in ((k_bits, k_mode, k_group, True),
+                                    (v_bits, v_mode, v_group, False)):
+        rowb = 4 * words_per_row(bits, head_dim)
+        if mode == ASYM_PER_CHANNEL:
+            nq = (seq_len // group) * group
+            total += streams * (nq * rowb + (nq // group) * head_dim * 4
+                                + (seq_len - nq) * head_dim * 2)
+            rows = nq
+        else:
+            meta = 2 if mode == SYM_PER_TOKEN else 4
+            total += streams * seq_len * (rowb + (head_dim // group) * meta)
+            rows = seq_len
+        if outliers_per_row:
+            total += streams * (4 * (rows + 1) + rows * outliers_per_row * 4)
+    return total
+
+
+# ---------------------------------------------------------------------------
+# Dense-and-sparse split: per-row top-k outliers
+# ---------------------------------------------------------------------------
+
+def select_outliers(rows16, k):
+    """Largest-magnitude entries of each row, kept aside in fp16.
+
+    [KVQuant] §2.2 item 3 splits each vector into a dense low-bit part and a
+    few full-precision outliers whose count per token is bounded; §3.3 sets
+    the ratio near 1 %. Reading R9: exactly ``k`` entries per (token, head)
+    row, ranked by |x| descending, ties to the lower channel, stored sorted
+    by channel.
+
+    Returns (mask [..., D] bool, cols [..., k] int64 ascending, vals [..., k]
+    float16).
+    """
+    rows16 = np.asarray(rows16, dtype=np.float16)
+    shape = rows16.shape
+    d = shape[-1]
+    flat = rows16.reshape(-1, d)
+    mask = np.zeros(flat.shape, dtype=bool)
+    if k == 0:
+        return (mask.reshape(shape), np.zeros(shape[:-1] + (0,), np.int64),
+                np.zeros(shape[:-1] + (0,), np.float16))
+    mag = np.abs(flat.astype(np.float32))
+    # stable sort on -|x| keeps equal magnitudes in channel order
+    order = np.argsort(-mag, axis=1, kind="stable")[:, :k]
+    cols = np.sort(order, axis=1)
+    np.put_along_axis(mask, cols, True, axis=1)
+    vals = np.take_along_axis(flat, cols, axis=1)
+    return (mask.reshape(shape), cols.reshape(shape[:-1] + (k,)),
+            vals.reshape(shape[:-1] + (k,)))
+
+
+# ---------------------------------------------------------------------------
+# Group quantizers (groups along the LAST axis)
+# ---------------------------------------------------------------------------
+
+def quantize_asym(x16, bits, mask=None):
+    """Asymmetric min/max quantizer over groups laid along the last axis.
+
+    [TurboQuant-3bit] §3.1: offset = group minimum, code =
+    clamp(round((x - offset) / scale), 0, 2^b - 1). Reading R1: scale =
+    (max - min) / (2^b - 1). Reading R4/R5: scale and offset are rounded to
+    fp16 (RNE) first and the codes are computed from the stored fp16 values,
+    in fp32: subtract, IEEE divide, round half to even, clamp. Reading R6: a
+    group whose scale is 0 (constant group, or fp16 underflow) gets code 0
+    everywhere; a group whose members are all outliers stores scale = zero
+    point = 0. Masked (outlier) slots are left out of the statistics and get
+    code 0 (reading R10).
+
+    Returns codes (int64, same shape), s16 and z16 (float16, shape[:-1]).
+    """
+    x16 = np.asarray(x16, dtype=np.float16)
+    x = x16.astype(np.float32)
+    if mask is None:
+        mask = np.zeros(x.shape, dtype=bool)
+    live = ~mask
+    any_live = live.any(axis=-1)
+    mn = np.where(live, x, np.float32(np.inf)).min(axis=-1)
+    mx = np.where(live, x, np.float32(-np.inf)).max(axis=-1)
+    mn = np.where(any_live, mn, np.float32(0))
+    mx = np.where(any_live, mx, np.float32(0))
+    levels = np.float32(2 ** bits - 1)
+    s32 = (mx - mn) / levels
+    s16 = s32.astype(np.float16)
+    z16 = mn.astype(np.float16)
+    s = s16.astype(np.float32)[..., None]
+    z = z16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint((x - z) / s)
+    q = np.where(s > 0, q, np.float32(0))
+    q = np.clip(q, 0, 2 ** bits - 1)
+    q = np.where(mask, 0, q)
+    return q.astype(np.int64), s16, z16
+
+
+def quantize_sym(x16, bits, mask=None):
+    """Symmetric quantizer with zero point 0 over groups along the last axis.
+
+    [NIAH-q8_0] §1.2: the q8_0 cache is int8 with zero point fixed at 0.
+    Reading R2: one fp16 scale per group of G channels, scale =
+    absmax / (2^(b-1) - 1). Reading R3: codes are clamped to the symmetric
+    range [-(2^(b-1) - 1), 2^(b-1) - 1] (inside the int8 range [-128, 127]).
+    Codes are computed from the stored fp16 scale in fp32 (IEEE divide,
+    round half to even).
+    """
+    x16 = np.asarray(x16, dtype=np.float16)
+    x = x16.astype(np.float32)
+    if mask is None:
+        mask = np.zeros(x.shape, dtype=bool)
+    qmax = 2 ** (bits - 1) - 1
+    am = np.where(mask, np.float32(0), np.abs(x)).max(axis=-1)
+    s32 = am / np.float32(qmax)
+    s16 = s32.astype(np.float16)
+    s = s16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.rint(x / s)
+    q = np.where(s > 0, q, np.float32(0))
+    q = np.clip(q, -qmax, qmax)
+    q = np.where(mask, 0, q)
+    return q.astype(np.int64), s16
+
+
+# ---------------------------------------------------------------------------
+# Bit packing along a (token, head) row
+# ---------------------------------------------------------------------------
+
+def pack_row_codes(codes, bits):
+    """Pack integer codes laid along the last axis into uint32 words.
+
+    Code j of a row goes to word j // cpw at bit offset (j % cpw) * b, with
+    cpw = 32/b for b in {4, 8} and cpw = 10 for b = 3 (ten codes per word,
+    the top two bits zero). Signed codes are stored as b-bit two's
+    complement. Rows shorter than a whole word leave the unused bits zero.
+    """
+    codes = np.asarray(codes, dtype=np.int64)
+    cpw = codes_per_word(bits)
+    d = codes.shape[-1]
+    nw = -(-d // cpw)
+    padded = np.zeros(codes.shape[:-1] + (nw * cpw,), dtype=np.uint64)
+    padded[..., :d] = (codes & ((1 << bits) - 1)).astype(np.uint64)
+    padded = padded.reshape(codes.shape[:-1] + (nw, cpw))
+    shifts = (np.arange(cpw, dtype=np.uint64) * np.uint64(bits))
+    words = (padded << shifts).sum(axis=-1)
+    return words.astype(np.uint32)
+
+
+def unpack_row_codes(words, bits, head_dim, signed=False):
+    """Inverse of :func:`pack_row_codes`."""
+    words = np.asarray(words, dtype=np.uint32).astype(np.uint64)
+    cpw = codes_per_word(bits)
+    shifts = np.arange(cpw, dtype=np.uint64) * np.uint64(bits)
+    c = (words[..., None] >> shifts) & np.uint64((1 << bits) - 1)
+    c = c.reshape(words.shape[:-1] + (-1,))[..., :head_dim].astype(np.int64)
+    if signed:
+        c = np.where(c >= (1 << (bits - 1)), c - (1 << bits), c)
+    return c
+
+
+# ---------------------------------------------------------------------------
+# Cache state for a batch of independent (batch, kv-head) streams
+# ---------------------------------------------------------------------------
+
+@dataclass
+class CodecSpec:
+    head_dim: int
+    k_bits: int
+    v_bits: int
+    k_mode: int
+    v_mode: int
+    k_group: int
+    v_group: int
+    outliers_per_row: int = 0
+
+
+@dataclass
+class TensorState:
+    """Quantized rows of one tensor (K or V) for N streams.
+
+    codes: int64 [N][R][D]; scale16/zero16: float16 metadata, per token
+    [N][R][D/G] or per channel block [N][R/T][D]; out_cols/out_vals:
+    [N][R][k]; resid: float16 [N][r][D] keys awaiting a full block.
+    """
+    codes: np.ndarray
+    scale16: np.ndarray
+    zero16: np.ndarray | None
+    out_cols: np.ndarray
+    out_vals: np.ndarray
+    resid: np.ndarray | None = None
+
+
+def _quantize_rows_per_token(x16, bits, mode, group, k_out):
+    n, r, d = x16.shape
+    mask, cols, vals = select_outliers(x16, k_out)
+    xg = x16.reshape(n, r, d // group, group)
+    mg = mask.reshape(n, r, d // group, group)
+    if mode == SYM_PER_TOKEN:
+        c, s16 = quantize_sym(xg, bits, mg)
+        z16 = None
+    else:
+        c, s16, z16 = quantize_asym(xg, bits, mg)
+    return c.reshape(n, r, d), s16, z16, cols, vals
+
+
+def _quantize_blocks_per_channel(x16, bits, block, k_out):
+    """Keys grouped per channel over ``block`` consecutive tokens
+    ([KVQuant] §2.2 item 1: per-channel key quantization; [W4A8-FA3] §2.4:
+    per-head groups of 64 positions, each with its own scale and zero point).
+    x16: [N][nb*T][D]."""
+    n, r, d = x16.shape
+    nb = r // block
+    mask, cols, vals = select_outliers(x16, k_out)
+    xt = x16.reshape(n, nb, block, d).transpose(0, 1, 3, 2)      # [N][nb][D][T]
+    mt = mask.reshape(n, nb, block, d).transpose(0, 1, 3, 2)
+    c, s16, z16 = quantize_asym(xt, bits, mt)                     # s16: [N][nb][D]
+    c = c.transpose(0, 1, 3, 2).reshape(n, r, d)
+    return c, s16, z16, cols, vals
+
+
+class OracleCache:
+    """Quantized KV cache of N independent streams (one per (batch, kv-head))
+    of one layer, built by the same steps the pages describe for a decode
+    loop ([KVQuant] §3.4: quantize the new key/value, store codes plus fp16
+    outliers, dequantize on read and attend).
+
+    Keys in per-channel mode (reading R7): a prefill of S tokens quantizes
+    floor(S/T) whole blocks and keeps the last S mod T keys in fp16; appended
+    keys join that fp16 residual and a block is quantized once it holds T
+    keys; codes already written are never requantized. Values (and keys in
+    per-token modes) are quantized row by row as they arrive ([NIAH-q8_0]
+    §2.2: only the newly written row is quantized).
+    """
+
+    def __init__(self, spec: CodecSpec, n_streams: int):
+        self.spec = spec
+        self.n = n_streams
+        self.length = 0
+        self.k = None
+        self.v = None
+
+    # -- helpers --------------------------------------------------------
+    def _empty_state(self, bits, mode, group):
+        d = self.spec.head_dim
+        n = self.n
+        ko = self.spec.outliers_per_row
+        if mode == ASYM_PER_CHANNEL:
+            meta_shape = (n, 0, d)
+        else:
+            meta_shape = (n, 0, d // group)
+        return TensorState(
+            codes=np.zeros((n, 0, d), np.int64),
+            scale16=np.zeros(meta_shape, np.float16),
+            zero16=None if mode == SYM_PER_TOKEN else np.zeros(meta_shape, np.float16),
+            out_cols=np.zeros((n, 0, ko), np.int64),
+            out_vals=np.zeros((n, 0, ko), np.float16),
+            resid=np.zeros((n, 0, d), np.float16) if mode == ASYM_PER_CHANNEL else None)
+
+    def _append_rows(self, st, x16, bits, mode, group):
+        ko = self.spec.outliers_per_row
+        if mode == ASYM_PER_CHANNEL:
+            pend = np.concatenate([st.resid, x16], axis=1)
+            nfull = (pend.shape[1] // group) * group
+            if nfull:
+                c, s16, z16, cols, vals = _quantize_blocks_per_channel(
+                    pend[:, :nfull], bits, group, ko)
+                st.codes = np.concatenate([st.codes, c], axis=1)
+                st.scale16 = np.concatenate([st.scale16, s16], axis=1)
+                st.zero16 = np.concatenate([st.zero16, z16], axis=1)
+                st.out_cols = np.concatenate([st.out_cols, cols], axis=1)
+                st.out_vals = np.concatenate([st.out_vals, vals], axis=1)
+            st.resid = pend[:, nfull:].copy()
+        else:
+            c, s16, z16, cols, vals = _quantize_rows_per_token(x16, bits, mode, group, ko)
+            st.codes = np.concatenate([st.codes, c], axis=1)
+            st.scale16 = np.concatenate([st.scale16, s16], axis=1)
+            if z16 is not None:
+                st.zero16 = np.concatenate([st.zero16, z16], axis=1)
+            st.out_cols = np.concatenate([st.out_cols, cols], axis=1)
+            st.out_vals = np.concatenate([st.out_vals, vals], axis=1)
+
+    # -- the decode-loop steps -------------------------------------------
+    def prefill(self, k16, v16):
+        """Quantize a whole prompt: k16, v16 float16 [N][S][D]."""
+        sp = self.spec
+        k16 = np.asarray(k16, np.float16)
+        v16 = np.asarray(v16, np.float16)
+        assert k16.shape == v16.shape and k16.shape[0] == self.n
+        assert k16.shape[2] == sp.head_dim
+        self.k = self._empty_state(sp.k_bits, sp.k_mode, sp.k_group)
+        self.v = self._empty_state(sp.v_bits, sp.v_mode, sp.v_group)
+        self._append_rows(self.k, k16, sp.k_bits, sp.k_mode, sp.k_group)
+        self._append_rows(self.v, v16, sp.v_bits, sp.v_mode, sp.v_group)
+        self.length = k16.shape[1]
+
+    def append(self, k1, v1):
+        """Quantize one new token per stream: k1, v1 float16 [N][D]."""
+        sp = self.spec
+        if self.k is None:
+            self.k = self._empty_state(sp.k_bits, sp.k_mode, sp.k_group)
+            self.v = self._empty_state(sp.v_bits, sp.v_mode, sp.v_group)
+        k1 = np.asarray(k1, np.float16)[:, None, :]
+        v1 = np.asarray(v1, np.float16)[:, None, :]
+        self._append_rows(self.k, k1, sp.k_bits, sp.k_mode, sp.k_group)
+        self._append_rows(self.v, v1, sp.v_bits, sp.v_mode, sp.v_group)
+        self.length += 1
+
+    # -- dequantization (fp64) --------------------------------------------
+    def _dequant(self, st, mode, group):
+        """x_hat = z16 + c * s16 (asymmetric) or c * s16 (symmetric), exact
+        in fp64; outlier slots take their stored fp16 value (reading R10);
+        fp16 residual keys are used as they are."""
+        d = self.spec.head_dim
+        c = st.codes.astype(np.float64)
+        n, r, _ = c.shape
+        if mode == ASYM_PER_CHANNEL:
+            s = np.repeat(st.scale16.astype(np.float64), group, axis=1)
+            z = np.repeat(st.zero16.astype(np.float64), group, axis=1)
+            xh = z + c * s
+        else:
+            s = np.repeat(st.scale16.astype(np.float64), group, axis=2)
+            xh = c * s
+            if mode == ASYM_PER_TOKEN:
+                xh = np.repeat(st.zero16.astype(np.float64), group, axis=2) + xh
+        if st.out_cols.shape[-1]:
+            np.put_along_axis(xh, st.out_cols, st.out_vals.astype(np.float64), axis=2)
+        if st.resid is not None and st.resid.shape[1]:
+            xh = np.concatenate([xh, st.resid.astype(np.float64)], axis=1)
+        assert xh.shape == (n, self.length, d)
+        return xh
+
+    def dequant_k(self):
+        return self._dequant(self.k, self.spec.k_mode, self.spec.k_group)
+
+    def dequant_v(self):
+        return self._dequant(self.v, self.spec.v_mode, self.spec.v_group)
+
+    def decode(self, q, softmax_scale):
+        """Decode attention of q [N][g][D] (g query heads per KV stream)
+        over every cached token of each stream, on the dequantized cache."""
+        if self.length == 0:
+            raise ValueError("attention over an empty cache is undefined")
+        return attend(q, self.dequant_k(), self.dequant_v(), softmax_scale)
+
+    # -- packed views in the storage format --------------------------------
+    def k_words(self):
+        return pack_row_codes(self.k.codes, self.spec.k_bits)
+
+    def v_words(self):
+        return pack_row_codes(self.v.codes, self.spec.v_bits)
+
+    @staticmethod
+    def csr(st):
+        """(row_ptr int32 [R+1], col uint16 [nnz], val float16 [nnz]) for
+        every stream, as arrays with a leading stream axis."""
+        n, r, k = st.out_cols.shape
+        row_ptr = np.broadcast_to((np.arange(r + 1) * k).astype(np.int32), (n, r + 1))
+        return (np.ascontiguousarray(row_ptr),
+                st.out_cols.reshape(n, r * k).astype(np.uint16),
+                st.out_vals.reshape(n, r * k))
+
+
+# ---------------------------------------------------------------------------
+# Attention (fp64)
+# ---------------------------------------------------------------------------
+
+def attend(q, k_hat, v_hat, softmax_scale):
+    """Single-token softmax attention per KV stream, in fp64.
+
+    q: [N][g][D]; k_hat, v_hat: [N][S][D]. For each query head,
+    e_t = scale * <q, k_t>, p = softmax(e) (shifted by max e), o = sum_t p_t v_t
+    ([KVQuant] §3.4 step 3: attention on the dequantized cache; reading R14
+    maps query head h to KV head h // (H_q / H_kv)).
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k_hat = np.asarray(k_hat, dtype=np.float64)
+    v_hat = np.asarray(v_hat, dtype=np.float64)
+    e = np.einsum("ngd,nsd->ngs", q, k_hat) * float(softmax_scale)
+    e = e - e.max(axis=-1, keepdims=True)
+    p = np.exp(e)
+    p /= p.sum(axis=-1, keepdims=True)
+    return np.einsum("ngs,nsd->ngd", p, v_hat)
+
+
+def row_relative_error(o, o_ref):
+    """Per-row error: max_d |o - o_ref| / max_d |o_ref| (reading R13)."""
+    o = np.asarray(o, np.float64)
+    o_ref = np.asarray(o_ref, np.float64)
+    num = np.abs(o - o_ref).max(axis=-1)
+    den = np.maximum(np.abs(o_ref).max(axis=-1), 1e-30)
+    return num / den
+
