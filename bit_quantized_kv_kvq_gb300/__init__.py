@@ -1,0 +1,230 @@
+"""Group-wise low-bit KV cache with fused dequant decode attention on GB300.
+
+A thin ctypes binding over ``libkvq.so`` (C ABI in ``include/kvq.h``). The
+binding only marshals arguments: every step of quantization and attention
+runs in the library's CUDA kernels. PyTorch provides device memory and
+streams. There is no CPU fallback: if the library is missing the import of
+:func:`lib` raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "KVQError", "QuantizedKVCache", "lib", "library_path",
+    "SYM_PER_TOKEN", "ASYM_PER_TOKEN", "ASYM_PER_CHANNEL", "F32", "F16",
+]
+
+SYM_PER_TOKEN = 0
+ASYM_PER_TOKEN = 1
+ASYM_PER_CHANNEL = 2
+F32 = 0
+F16 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+library_path = os.path.join(_HERE, "libkvq.so")
+
+STATUS_NAMES = {
+    0: "KVQ_OK", 1: "KVQ_ERR_INVALID_ARG", 2: "KVQ_ERR_UNSUPPORTED",
+    3: "KVQ_ERR_BUFFER_TOO_SMALL", 4: "KVQ_ERR_CAPACITY", 5: "KVQ_ERR_CUDA",
+    6: "KVQ_ERR_TIMEOUT", 7: "KVQ_ERR_DEVICE_STATUS",
+}
+
+
+class KVQError(RuntimeError):
+    def __init__(self, status, message):
+        self.status = status
+        super().__init__("%s: %s" % (STATUS_NAMES.get(status, str(status)), message))
+
+
+class Config(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "num_layers", "batch", "num_kv_heads", "head_dim", "max_seq", "k_bits", "v_bits",
+        "k_mode", "v_mode", "k_group", "v_group", "outliers_per_row")]
+
+
+class Layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "capacity", "length", "k_quantized_len", "k_resid_len", "k_words_per_row",
+        "v_words_per_row", "k_meta_entry_bytes", "v_meta_entry_bytes")] + [
+        (n, ctypes.c_int64) for n in (
+            "k_codes_stream_bytes", "v_codes_stream_bytes", "k_meta_stream_bytes",
+            "v_meta_stream_bytes", "k_resid_stream_bytes", "out_rowptr_stream_bytes",
+            "out_col_stream_bytes", "out_val_stream_bytes")] + [
+        (n, ctypes.c_void_p) for n in (
+            "k_codes", "k_meta", "k_resid", "v_codes", "v_meta", "k_out_rowptr", "k_out_col",
+            "k_out_val", "v_out_rowptr", "v_out_col", "v_out_val")]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int32
+_SIGNATURES = {
+    "kvq_cache_bytes": [ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_size_t)],
+    "kvq_cache_create": [ctypes.POINTER(Config), _P, ctypes.c_size_t, _P, ctypes.POINTER(_P)],
+    "kvq_cache_destroy": [_P],
+    "kvq_prefill_quantize": [_P, _I, _P, _P, _I, _P],
+    "kvq_append_quantize": [_P, _I, _P, _P, _P],
+    "kvq_decode_workspace_bytes": [_P, _I, ctypes.POINTER(ctypes.c_size_t)],
+    "kvq_decode_attention": [_P, _I, _P, _I, ctypes.c_float, _P, _I, _P, ctypes.c_size_t, _P],
+    "kvq_cache_set_decode_splits": [_P, _I],
+    "kvq_cache_get_layout": [_P, _I, ctypes.POINTER(Layout)],
+    "kvq_cache_length": [_P, _I, ctypes.POINTER(_I)],
+    "kvq_cache_status": [_P, _P, ctypes.POINTER(ctypes.c_uint32)],
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(library_path):
+            raise ImportError("libkvq.so is not built (run __graft_entry__.build()); "
+                              "there is no fallback implementation")
+        L = ctypes.CDLL(library_path)
+        for name, args in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        L.kvq_last_error.argtypes = []
+        L.kvq_last_error.restype = ctypes.c_char_p
+        L.kvq_version.argtypes = []
+        L.kvq_version.restype = ctypes.c_int32
+        _lib = L
+    return _lib
+
+
+def check(status):
+    if status != 0:
+        raise KVQError(status, lib().kvq_last_error().decode(errors="replace"))
+
+
+def _stream_ptr(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def make_config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits, k_mode,
+                v_mode, k_group, v_group, outliers_per_row=0):
+    return Config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits, k_mode,
+                  v_mode, k_group, v_group, outliers_per_row)
+
+
+def cache_bytes(cfg: Config) -> int:
+    n = ctypes.c_size_t()
+    check(lib().kvq_cache_bytes(ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def _check_half(t, shape, name):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.float16 or not t.is_cuda:
+        raise TypeError("%s must be a CUDA float16 tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError("%s has shape %s, expected %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+class QuantizedKVCache:
+    """A packed KV cache of ``num_layers`` layers in one torch-owned device
+    buffer, driven through the C ABI."""
+
+    def __init__(self, num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits,
+                 k_mode, v_mode, k_group, v_group, outliers_per_row=0, device=None,
+                 stream=None):
+        self.cfg = make_config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits,
+                               v_bits, k_mode, v_mode, k_group, v_group, outliers_per_row)
+        self.nbytes = cache_bytes(self.cfg)
+        self.device = torch.device(device if device is not None else "cuda")
+        self.buffer = torch.empty(self.nbytes, dtype=torch.uint8, device=self.device)
+        h = ctypes.c_void_p()
+        check(lib().kvq_cache_create(ctypes.byref(self.cfg), ctypes.c_void_p(self.buffer.data_ptr()),
+                                     self.nbytes, _stream_ptr(stream), ctypes.byref(h)))
+        self.handle = h
+        self._ws = {}
+
+    # -- hot path -----------------------------------------------------------
+    def prefill(self, layer, k, v, stream=None):
+        c = self.cfg
+        s = k.shape[2] if k.dim() == 4 else 0
+        _check_half(k, (c.batch, c.num_kv_heads, s, c.head_dim), "k")
+        _check_half(v, (c.batch, c.num_kv_heads, s, c.head_dim), "v")
+        check(lib().kvq_prefill_quantize(self.handle, layer, ctypes.c_void_p(k.data_ptr()),
+                                         ctypes.c_void_p(v.data_ptr()), s, _stream_ptr(stream)))
+
+    def append(self, layer, k1, v1, stream=None):
+        c = self.cfg
+        _check_half(k1, (c.batch, c.num_kv_heads, c.head_dim), "k1")
+        _check_half(v1, (c.batch, c.num_kv_heads, c.head_dim), "v1")
+        check(lib().kvq_append_quantize(self.handle, layer, ctypes.c_void_p(k1.data_ptr()),
+                                        ctypes.c_void_p(v1.data_ptr()), _stream_ptr(stream)))
+
+    def workspace_bytes(self, num_q_heads):
+        n = ctypes.c_size_t()
+        check(lib().kvq_decode_workspace_bytes(self.handle, num_q_heads, ctypes.byref(n)))
+        return n.value
+
+    def workspace(self, num_q_heads):
+        ws = self._ws.get(num_q_heads)
+        if ws is None:
+            ws = torch.empty(self.workspace_bytes(num_q_heads), dtype=torch.uint8, device=self.device)
+            self._ws[num_q_heads] = ws
+        return ws
+
+    def decode(self, layer, q, softmax_scale, out=None, out_dtype=torch.float32, workspace=None,
+               stream=None):
+        c = self.cfg
+        hq = q.shape[1]
+        _check_half(q, (c.batch, hq, c.head_dim), "q")
+        if out is None:
+            out = torch.empty((c.batch, hq, c.head_dim), dtype=out_dtype, device=q.device)
+        code = {torch.float32: F32, torch.float16: F16}[out.dtype]
+        ws = self.workspace(hq) if workspace is None else workspace
+        check(lib().kvq_decode_attention(self.handle, layer, ctypes.c_void_p(q.data_ptr()), hq,
+                                         float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
+                                         code, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                         _stream_ptr(stream)))
+        return out
+
+    # -- inspection ---------------------------------------------------------
+    def set_decode_splits(self, splits):
+        check(lib().kvq_cache_set_decode_splits(self.handle, splits))
+
+    def length(self, layer):
+        n = ctypes.c_int32()
+        check(lib().kvq_cache_length(self.handle, layer, ctypes.byref(n)))
+        return n.value
+
+    def layout(self, layer):
+        lo = Layout()
+        check(lib().kvq_cache_get_layout(self.handle, layer, ctypes.byref(lo)))
+        return lo
+
+    def status(self, stream=None):
+        w = ctypes.c_uint32()
+        check(lib().kvq_cache_status(self.handle, _stream_ptr(stream), ctypes.byref(w)))
+        return w.value
+
+    def view(self, ptr, nbytes, dtype):
+        """A tensor view of ``nbytes`` of the cache buffer starting at device
+        pointer ``ptr`` (for inspection and checkpoints)."""
+        off = int(ptr) - self.buffer.data_ptr()
+        if off < 0 or off + nbytes > self.nbytes:
+            raise ValueError("pointer outside the cache buffer")
+        return self.buffer[off:off + nbytes].view(dtype)
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib().kvq_cache_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,8 @@
+// Decode-kernel instantiations for 1 query head(s) per kv-head.
+#include "decode_impl.cuh"
+
+namespace kvq {
+cudaError_t launch_decode_g1(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
+  return launch_decode_g<1>(L, a, st);
+}
+}  // namespace kvq

@@ -1,0 +1,452 @@
+// Host side of the C ABI declared in include/kvq.h: configuration checks,
+// the packed layout inside the caller's buffer, split planning and launch
+// dispatch. No device memory is allocated here.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "kvq_internal.h"
+
+namespace {
+
+thread_local std::string g_err;
+
+kvq_status fail(kvq_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+kvq_status fail(kvq_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+kvq_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(KVQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
+
+int codes_per_word(int bits) { return bits == 3 ? 10 : 32 / bits; }
+
+int words_per_row(int bits) {
+  const int cpw = codes_per_word(bits);
+  return (kvq::kHeadDim + cpw - 1) / cpw;
+}
+
+// Byte layout of one layer; all offsets relative to the layer base.
+struct TensorPlan {
+  int64_t codes_off = 0, codes_sb = 0;
+  int64_t meta_off = 0, meta_sb = 0;
+  int64_t resid_off = 0, resid_sb = 0;
+  int64_t rp_off = 0, rp_sb = 0;
+  int64_t col_off = 0, col_sb = 0;
+  int64_t val_off = 0, val_sb = 0;
+  int meta_bytes = 0;
+  int words = 0;
+};
+
+struct Plan {
+  int capacity = 0;
+  int64_t n_streams = 0;
+  TensorPlan k, v;
+  int64_t layer_bytes = 0;
+  int64_t header_bytes = 256;
+  int64_t total = 0;
+};
+
+kvq_status check_tensor(const char* name, int bits, int mode, int group, bool is_k) {
+  if (bits != 3 && bits != 4 && bits != 8)
+    return fail(KVQ_ERR_INVALID_ARG, "%s_bits must be 3, 4 or 8 (got %d)", name, bits);
+  if (mode < KVQ_SYM_PER_TOKEN || mode > KVQ_ASYM_PER_CHANNEL)
+    return fail(KVQ_ERR_INVALID_ARG, "%s_mode %d is not a kvq_mode", name, mode);
+  if (mode == KVQ_ASYM_PER_CHANNEL) {
+    if (!is_k)
+      return fail(KVQ_ERR_UNSUPPORTED, "per-channel grouping is supported for keys only");
+    if (group != 64 && group != 128 && group != 256)
+      return fail(KVQ_ERR_UNSUPPORTED, "%s_group (tokens per block) must be 64, 128 or 256 (got %d)",
+                  name, group);
+    return KVQ_OK;
+  }
+  if (mode == KVQ_SYM_PER_TOKEN && bits != 8)
+    return fail(KVQ_ERR_UNSUPPORTED, "symmetric groups are supported at 8 bits only");
+  if (group != 16 && group != 32 && group != 64 && group != 128)
+    return fail(KVQ_ERR_INVALID_ARG, "%s_group must be 16, 32, 64 or 128 channels (got %d)", name,
+                group);
+  if (group != kvq::kHeadDim && group % codes_per_word(bits) != 0)
+    return fail(KVQ_ERR_UNSUPPORTED,
+                "%s_group %d is not a multiple of the %d codes per word (3-bit groups must span "
+                "the whole row)",
+                name, group, codes_per_word(bits));
+  return KVQ_OK;
+}
+
+kvq_status check_config(const kvq_config* c) {
+  if (!c) return fail(KVQ_ERR_INVALID_ARG, "config is NULL");
+  if (c->num_layers < 1 || c->batch < 1 || c->num_kv_heads < 1 || c->max_seq < 1)
+    return fail(KVQ_ERR_INVALID_ARG, "num_layers, batch, num_kv_heads and max_seq must be >= 1");
+  if (c->head_dim != kvq::kHeadDim)
+    return fail(KVQ_ERR_UNSUPPORTED, "head_dim must be 128 (got %d)", c->head_dim);
+  if (c->max_seq > (1 << 24))
+    return fail(KVQ_ERR_UNSUPPORTED, "max_seq above 16M tokens is not supported");
+  if ((int64_t)c->batch * c->num_kv_heads > 65535)
+    return fail(KVQ_ERR_UNSUPPORTED, "batch * num_kv_heads must be <= 65535");
+  if (c->outliers_per_row < 0 || c->outliers_per_row > kvq::kMaxOutliers)
+    return fail(KVQ_ERR_INVALID_ARG, "outliers_per_row must be in [0, %d]", kvq::kMaxOutliers);
+  kvq_status s = check_tensor("k", c->k_bits, c->k_mode, c->k_group, true);
+  if (s != KVQ_OK) return s;
+  return check_tensor("v", c->v_bits, c->v_mode, c->v_group, false);
+}
+
+void plan_tensor(const kvq_config& c, int cap, bool is_k, int64_t* cursor, TensorPlan* t) {
+  const int bits = is_k ? c.k_bits : c.v_bits;
+  const int mode = is_k ? c.k_mode : c.v_mode;
+  const int group = is_k ? c.k_group : c.v_group;
+  const int64_t n = (int64_t)c.batch * c.num_kv_heads;
+  const int D = kvq::kHeadDim;
+  t->words = words_per_row(bits);
+  t->meta_bytes = mode == KVQ_SYM_PER_TOKEN ? 2 : 4;
+  auto take = [&](int64_t stream_bytes, int64_t* off, int64_t* sb) {
+    *sb = round_up(stream_bytes, 16);
+    *off = *cursor;
+    *cursor = round_up(*cursor + n * *sb, 256);
+  };
+  take((int64_t)cap * t->words * 4, &t->codes_off, &t->codes_sb);
+  if (mode == KVQ_ASYM_PER_CHANNEL) {
+    take((int64_t)(cap / group) * D * 4, &t->meta_off, &t->meta_sb);
+    take((int64_t)group * D * 2, &t->resid_off, &t->resid_sb);
+  } else {
+    take((int64_t)cap * (D / group) * t->meta_bytes, &t->meta_off, &t->meta_sb);
+  }
+  if (c.outliers_per_row > 0) {
+    take((int64_t)(cap + 4) * 4, &t->rp_off, &t->rp_sb);
+    take((int64_t)cap * c.outliers_per_row * 2, &t->col_off, &t->col_sb);
+    take((int64_t)cap * c.outliers_per_row * 2, &t->val_off, &t->val_sb);
+  }
+}
+
+Plan make_plan(const kvq_config& c) {
+  Plan p;
+  int64_t gran = kvq::kTile;
+  if (c.k_mode == KVQ_ASYM_PER_CHANNEL && c.k_group > gran) gran = c.k_group;
+  p.capacity = (int)round_up(c.max_seq, gran);
+  p.n_streams = (int64_t)c.batch * c.num_kv_heads;
+  int64_t cursor = 0;
+  plan_tensor(c, p.capacity, true, &cursor, &p.k);
+  plan_tensor(c, p.capacity, false, &cursor, &p.v);
+  p.layer_bytes = cursor;
+  p.total = p.header_bytes + p.layer_bytes * c.num_layers;
+  return p;
+}
+
+}  // namespace
+
+struct kvq_cache {
+  kvq_config cfg;
+  Plan plan;
+  unsigned char* base = nullptr;
+  size_t bytes = 0;
+  std::vector<int> len;
+  int splits_override = 0;
+  int sm_count = 0;
+};
+
+namespace {
+
+kvq::TensorDev tensor_dev(const kvq_cache* h, int layer, bool is_k) {
+  const kvq_config& c = h->cfg;
+  const TensorPlan& t = is_k ? h->plan.k : h->plan.v;
+  unsigned char* lb = h->base + h->plan.header_bytes + (int64_t)layer * h->plan.layer_bytes;
+  kvq::TensorDev d;
+  d.bits = is_k ? c.k_bits : c.v_bits;
+  d.mode = is_k ? c.k_mode : c.v_mode;
+  d.group = is_k ? c.k_group : c.v_group;
+  d.words = t.words;
+  d.meta_bytes = t.meta_bytes;
+  d.codes = reinterpret_cast<uint32_t*>(lb + t.codes_off);
+  d.codes_sstride = t.codes_sb / 4;
+  d.meta = lb + t.meta_off;
+  d.meta_sstride = t.meta_sb;
+  d.resid = d.mode == KVQ_ASYM_PER_CHANNEL ? reinterpret_cast<__half*>(lb + t.resid_off) : nullptr;
+  d.resid_sstride = t.resid_sb / 2;
+  const bool out = c.outliers_per_row > 0;
+  d.rowptr = out ? reinterpret_cast<int32_t*>(lb + t.rp_off) : nullptr;
+  d.rowptr_sstride = t.rp_sb / 4;
+  d.col = out ? reinterpret_cast<uint16_t*>(lb + t.col_off) : nullptr;
+  d.val = out ? reinterpret_cast<__half*>(lb + t.val_off) : nullptr;
+  d.out_sstride = t.col_sb / 2;
+  return d;
+}
+
+kvq::LayerDev layer_dev(const kvq_cache* h, int layer) {
+  kvq::LayerDev L;
+  L.k = tensor_dev(h, layer, true);
+  L.v = tensor_dev(h, layer, false);
+  L.n_streams = (int)h->plan.n_streams;
+  L.num_kv_heads = h->cfg.num_kv_heads;
+  L.capacity = h->plan.capacity;
+  L.outliers = h->cfg.outliers_per_row;
+  L.status = reinterpret_cast<uint32_t*>(h->base);
+  return L;
+}
+
+int k_quant_len(const kvq_config& c, int len) {
+  if (c.k_mode != KVQ_ASYM_PER_CHANNEL) return len;
+  return len / c.k_group * c.k_group;
+}
+
+// Splits: enough CTAs for about two waves of 4 CTAs per SM, at least one
+// 64-token tile per split.
+void plan_splits(const kvq_cache* h, int len, int* splits, int* tiles_per_split) {
+  const int ntiles = (len + kvq::kTile - 1) / kvq::kTile;
+  int want;
+  if (h->splits_override > 0) {
+    want = h->splits_override;
+  } else {
+    const int64_t target = (int64_t)h->sm_count * 8;
+    want = (int)((target + h->plan.n_streams - 1) / h->plan.n_streams);
+  }
+  if (want < 1) want = 1;
+  if (want > ntiles) want = ntiles;
+  int tps = (ntiles + want - 1) / want;
+  *tiles_per_split = tps;
+  *splits = (ntiles + tps - 1) / tps;
+}
+
+size_t workspace_for(const kvq_cache* h, int num_q_heads, int splits) {
+  const int64_t rows = (int64_t)h->cfg.batch * num_q_heads;
+  return (size_t)(rows * splits * kvq::kHeadDim * 4 + round_up(rows * splits * 2 * 4, 256) + 256);
+}
+
+kvq_status check_layer(const kvq_cache* h, int layer) {
+  if (!h) return fail(KVQ_ERR_INVALID_ARG, "cache handle is NULL");
+  if (layer < 0 || layer >= h->cfg.num_layers)
+    return fail(KVQ_ERR_INVALID_ARG, "layer %d out of range [0, %d)", layer, h->cfg.num_layers);
+  return KVQ_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes) {
+  if (!bytes) return fail(KVQ_ERR_INVALID_ARG, "bytes is NULL");
+  kvq_status s = check_config(cfg);
+  if (s != KVQ_OK) return s;
+  *bytes = (size_t)make_plan(*cfg).total;
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_create(const kvq_config* cfg, void* dev_buf, size_t bytes, void* stream,
+                            kvq_cache** out) {
+  if (!out) return fail(KVQ_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  kvq_status s = check_config(cfg);
+  if (s != KVQ_OK) return s;
+  if (!dev_buf) return fail(KVQ_ERR_INVALID_ARG, "dev_buf is NULL");
+  if (!aligned(dev_buf, 256)) return fail(KVQ_ERR_INVALID_ARG, "dev_buf must be 256-byte aligned");
+  Plan p = make_plan(*cfg);
+  if ((int64_t)bytes < p.total)
+    return fail(KVQ_ERR_BUFFER_TOO_SMALL, "cache buffer has %zu bytes, needs %lld", bytes,
+                (long long)p.total);
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, dev_buf);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+  if (attr.type != cudaMemoryTypeDevice && attr.type != cudaMemoryTypeManaged)
+    return fail(KVQ_ERR_INVALID_ARG, "dev_buf is not device memory");
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, attr.device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  e = cudaMemsetAsync(dev_buf, 0, (size_t)p.total, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  kvq_cache* h = new kvq_cache;
+  h->cfg = *cfg;
+  h->plan = p;
+  h->base = static_cast<unsigned char*>(dev_buf);
+  h->bytes = bytes;
+  h->len.assign(cfg->num_layers, 0);
+  h->sm_count = sms > 0 ? sms : 1;
+  *out = h;
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_destroy(kvq_cache* cache) {
+  delete cache;
+  return KVQ_OK;
+}
+
+kvq_status kvq_prefill_quantize(kvq_cache* h, int32_t layer, const void* k, const void* v,
+                                int32_t seq_len, void* stream) {
+  kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  if (seq_len < 0) return fail(KVQ_ERR_INVALID_ARG, "seq_len must be >= 0");
+  if (seq_len > h->cfg.max_seq)
+    return fail(KVQ_ERR_CAPACITY, "seq_len %d exceeds max_seq %d", seq_len, h->cfg.max_seq);
+  if (seq_len > 0) {
+    if (!k || !v) return fail(KVQ_ERR_INVALID_ARG, "k and v must not be NULL");
+    if (!aligned(k, 16) || !aligned(v, 16))
+      return fail(KVQ_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  }
+  kvq::LayerDev L = layer_dev(h, layer);
+  cudaError_t e = kvq::launch_prefill(L, static_cast<const __half*>(k),
+                                      static_cast<const __half*>(v), seq_len,
+                                      static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  h->len[layer] = seq_len;
+  return KVQ_OK;
+}
+
+kvq_status kvq_append_quantize(kvq_cache* h, int32_t layer, const void* k, const void* v,
+                               void* stream) {
+  kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  if (!k || !v) return fail(KVQ_ERR_INVALID_ARG, "k and v must not be NULL");
+  if (!aligned(k, 16) || !aligned(v, 16))
+    return fail(KVQ_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+  const int pos = h->len[layer];
+  if (pos >= h->cfg.max_seq)
+    return fail(KVQ_ERR_CAPACITY, "layer %d is full (%d tokens)", layer, pos);
+  kvq::LayerDev L = layer_dev(h, layer);
+  cudaError_t e = kvq::launch_append(L, static_cast<const __half*>(k),
+                                     static_cast<const __half*>(v), pos,
+                                     static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  h->len[layer] = pos + 1;
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_workspace_bytes(const kvq_cache* h, int32_t num_q_heads, size_t* bytes) {
+  if (!h || !bytes) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
+  if (num_q_heads < 1) return fail(KVQ_ERR_INVALID_ARG, "num_q_heads must be >= 1");
+  const int max_splits = h->plan.capacity / kvq::kTile;  // one tile per split at most
+  *bytes = workspace_for(h, num_q_heads, max_splits);
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int32_t num_q_heads,
+                                float softmax_scale, void* out, int32_t out_dtype,
+                                void* workspace, size_t ws_bytes, void* stream) {
+  kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  if (!q || !out || !workspace) return fail(KVQ_ERR_INVALID_ARG, "q, out and workspace must not be NULL");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16))
+    return fail(KVQ_ERR_INVALID_ARG, "q, out and workspace must be 16-byte aligned");
+  if (out_dtype != KVQ_F32 && out_dtype != KVQ_F16)
+    return fail(KVQ_ERR_INVALID_ARG, "out_dtype must be KVQ_F32 or KVQ_F16");
+  const int hkv = h->cfg.num_kv_heads;
+  if (num_q_heads < hkv || num_q_heads % hkv != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
+                num_q_heads, hkv);
+  const int gqa = num_q_heads / hkv;
+  const int len = h->len[layer];
+  if (len == 0) return fail(KVQ_ERR_INVALID_ARG, "layer %d is empty: attention is undefined", layer);
+  kvq::LayerDev L = layer_dev(h, layer);
+  if (!kvq::decode_supported(L, gqa))
+    return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for this codec pair with %d query heads per kv-head",
+                gqa);
+  int splits = 1, tps = 1;
+  plan_splits(h, len, &splits, &tps);
+  const size_t need = workspace_for(h, num_q_heads, splits);
+  if (ws_bytes < need)
+    return fail(KVQ_ERR_BUFFER_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  kvq::DecodeArgs a;
+  a.q = static_cast<const __half*>(q);
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.num_q_heads = num_q_heads;
+  a.gqa = gqa;
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.length = len;
+  a.k_quant_len = k_quant_len(h->cfg, len);
+  a.splits = splits;
+  a.tiles_per_split = tps;
+  const int64_t rows = (int64_t)h->cfg.batch * num_q_heads;
+  a.part_o = static_cast<float*>(workspace);
+  a.part_ml = a.part_o + rows * splits * kvq::kHeadDim;
+  cudaError_t e = kvq::launch_decode(L, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_set_decode_splits(kvq_cache* h, int32_t splits) {
+  if (!h) return fail(KVQ_ERR_INVALID_ARG, "cache handle is NULL");
+  if (splits < 0) return fail(KVQ_ERR_INVALID_ARG, "splits must be >= 0");
+  h->splits_override = splits;
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_get_layout(const kvq_cache* h, int32_t layer, kvq_layout* o) {
+  kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  if (!o) return fail(KVQ_ERR_INVALID_ARG, "out is NULL");
+  std::memset(o, 0, sizeof *o);
+  const int len = h->len[layer];
+  kvq::LayerDev L = layer_dev(h, layer);
+  o->capacity = h->plan.capacity;
+  o->length = len;
+  o->k_quantized_len = k_quant_len(h->cfg, len);
+  o->k_resid_len = len - o->k_quantized_len;
+  o->k_words_per_row = h->plan.k.words;
+  o->v_words_per_row = h->plan.v.words;
+  o->k_meta_entry_bytes = h->plan.k.meta_bytes;
+  o->v_meta_entry_bytes = h->plan.v.meta_bytes;
+  o->k_codes_stream_bytes = h->plan.k.codes_sb;
+  o->v_codes_stream_bytes = h->plan.v.codes_sb;
+  o->k_meta_stream_bytes = h->plan.k.meta_sb;
+  o->v_meta_stream_bytes = h->plan.v.meta_sb;
+  o->k_resid_stream_bytes = h->plan.k.resid_sb;
+  o->out_rowptr_stream_bytes = h->plan.k.rp_sb;
+  o->out_col_stream_bytes = h->plan.k.col_sb;
+  o->out_val_stream_bytes = h->plan.k.val_sb;
+  o->k_codes = L.k.codes;
+  o->k_meta = L.k.meta;
+  o->k_resid = L.k.resid;
+  o->v_codes = L.v.codes;
+  o->v_meta = L.v.meta;
+  o->k_out_rowptr = L.k.rowptr;
+  o->k_out_col = L.k.col;
+  o->k_out_val = L.k.val;
+  o->v_out_rowptr = L.v.rowptr;
+  o->v_out_col = L.v.col;
+  o->v_out_val = L.v.val;
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_length(const kvq_cache* h, int32_t layer, int32_t* len) {
+  kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  if (!len) return fail(KVQ_ERR_INVALID_ARG, "len is NULL");
+  *len = h->len[layer];
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_status(kvq_cache* h, void* stream, uint32_t* word) {
+  if (!h) return fail(KVQ_ERR_INVALID_ARG, "cache handle is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  uint32_t w = 0;
+  e = cudaMemcpy(&w, h->base, sizeof w, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy status");
+  if (w != 0) {
+    e = cudaMemset(h->base, 0, sizeof w);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemset status");
+  }
+  if (word) *word = w;
+  if (w & kvq::kStatusTimeout) return fail(KVQ_ERR_TIMEOUT, "a bounded device wait gave up (status 0x%x)", w);
+  if (w) return fail(KVQ_ERR_DEVICE_STATUS, "device status word 0x%x", w);
+  return KVQ_OK;
+}
+
+const char* kvq_last_error(void) { return g_err.c_str(); }
+
+int32_t kvq_version(void) { return 100; }
+
+}  // extern "C"

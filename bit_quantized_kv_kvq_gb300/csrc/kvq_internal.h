@@ -1,0 +1,77 @@
+// Internal structures shared by the host API and the kernel launchers.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int kHeadDim = 128;   // channels per (token, head) row
+constexpr int kTile = 64;       // decode tile (tokens) and capacity granularity
+constexpr int kMaxOutliers = 8; // per (token, head) row
+
+// Device status bits (see kvq_cache_status).
+constexpr uint32_t kStatusTimeout = 1u << 0;
+constexpr uint32_t kStatusBadState = 1u << 1;
+
+// One tensor (K or V) of one layer, device side.
+struct TensorDev {
+  int bits;
+  int mode;             // kvq_mode
+  int group;            // channels (per-token) or tokens (per-channel)
+  int words;            // 32-bit words per (token, head) row
+  int meta_bytes;       // 2 (symmetric scale) or 4 (scale, zero)
+  uint32_t* codes;      // [n][cap][words]
+  int64_t codes_sstride;  // words between streams
+  unsigned char* meta;  // see kvq_layout
+  int64_t meta_sstride;   // bytes between streams
+  __half* resid;        // [n][group][D] (per-channel keys only)
+  int64_t resid_sstride;  // halves between streams
+  int32_t* rowptr;      // [n][cap + 4]
+  int64_t rowptr_sstride; // ints between streams
+  uint16_t* col;        // [n][cap * k]
+  __half* val;          // [n][cap * k]
+  int64_t out_sstride;  // entries between streams
+};
+
+struct LayerDev {
+  TensorDev k, v;
+  int n_streams;        // batch * num_kv_heads
+  int num_kv_heads;
+  int capacity;
+  int outliers;         // per row
+  uint32_t* status;
+};
+
+// Prefill of seq_len tokens: k, v fp16 [n][seq_len][D].
+cudaError_t launch_prefill(const LayerDev& L, const __half* k, const __half* v, int seq_len,
+                           cudaStream_t stream);
+
+// Append of one token at position pos (= length before the call): k1, v1
+// fp16 [n][D].
+cudaError_t launch_append(const LayerDev& L, const __half* k1, const __half* v1, int pos,
+                          cudaStream_t stream);
+
+struct DecodeArgs {
+  const __half* q;      // [B][Hq][D]
+  void* out;            // [B][Hq][D]
+  int out_dtype;
+  int num_q_heads;
+  int gqa;              // Hq / Hkv
+  float scale_log2;     // softmax_scale * log2(e)
+  int length;           // tokens cached
+  int k_quant_len;      // key rows held as codes
+  int splits;
+  int tiles_per_split;
+  float* part_o;        // [B*Hq][splits][D]
+  float* part_ml;       // [B*Hq][splits][2]
+};
+
+cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);
+
+bool decode_supported(const LayerDev& L, int gqa);
+
+}  // namespace kvq

@@ -1,0 +1,97 @@
+"""Host-only checks of the C-ABI library (no GPU needed): it loads, exports
+every entry point include/kvq.h declares, sizes caches, and rejects bad
+arguments before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import bit_quantized_kv_kvq_gb300 as kvq
+from bit_quantized_kv_kvq_gb300 import workloads as W
+from oracle import kvq_oracle as O
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    __graft_entry__.build()
+    return kvq.lib()
+
+
+def declared_entry_points():
+    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    return sorted(set(re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_entry_points()
+    assert len(names) >= 13
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert lib.kvq_version() == 100
+
+
+def _cfg(**kw):
+    base = dict(num_layers=1, batch=2, num_kv_heads=4, head_dim=128, max_seq=1000, k_bits=4,
+                v_bits=4, k_mode=kvq.ASYM_PER_CHANNEL, v_mode=kvq.ASYM_PER_TOKEN, k_group=64,
+                v_group=64, outliers_per_row=0)
+    base.update(kw)
+    return kvq.make_config(**base)
+
+
+@pytest.mark.parametrize("wl", W.ALL, ids=lambda w: w.name)
+def test_cache_bytes_cover_the_algorithmic_footprint(lib, wl):
+    max_seq = wl.seq_len + wl.decode_steps
+    cfg = kvq.make_config(wl.num_layers, wl.batch, wl.num_kv_heads, wl.head_dim, max_seq,
+                          wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group, wl.v_group,
+                          wl.outliers_per_row)
+    got = kvq.cache_bytes(cfg)
+    algo = O.packed_cache_bytes(wl.num_layers, wl.batch, wl.num_kv_heads, wl.head_dim, max_seq,
+                                wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group,
+                                wl.v_group, wl.outliers_per_row)
+    assert got >= algo
+    # capacity rounding to 64 tokens + the fp16 residual block + alignment
+    slack = wl.num_layers * wl.batch * wl.num_kv_heads * (64 + wl.k_group) * 600 + 4096 * wl.num_layers
+    assert got <= algo + slack, (got, algo)
+
+
+BAD = [
+    (dict(head_dim=64), 2), (dict(k_bits=5), 1), (dict(v_mode=kvq.ASYM_PER_CHANNEL), 2),
+    (dict(k_mode=kvq.SYM_PER_TOKEN, k_bits=4, k_group=32), 2), (dict(v_group=48), 1),
+    (dict(v_bits=3, v_group=64), 2), (dict(outliers_per_row=9), 1), (dict(k_group=32), 2),
+    (dict(max_seq=0), 1), (dict(batch=0), 1), (dict(k_mode=7), 1),
+]
+
+
+@pytest.mark.parametrize("kw,status", BAD, ids=[str(b[0]) for b in BAD])
+def test_bad_configs_are_rejected(lib, kw, status):
+    n = ctypes.c_size_t()
+    assert lib.kvq_cache_bytes(ctypes.byref(_cfg(**kw)), ctypes.byref(n)) == status
+    assert lib.kvq_last_error()
+
+
+def test_create_rejects_bad_buffers_on_the_host(lib):
+    cfg = _cfg()
+    h = ctypes.c_void_p()
+    assert lib.kvq_cache_create(ctypes.byref(cfg), None, 1 << 30, None, ctypes.byref(h)) == 1
+    assert lib.kvq_cache_create(ctypes.byref(cfg), ctypes.c_void_p(0x1008), 1 << 30, None,
+                                ctypes.byref(h)) == 1
+    assert lib.kvq_cache_create(ctypes.byref(cfg), ctypes.c_void_p(0x10000), 100, None,
+                                ctypes.byref(h)) == 3
+    assert b"needs" in lib.kvq_last_error()
+    assert h.value is None
+
+
+def test_null_handle_is_rejected(lib):
+    assert lib.kvq_prefill_quantize(None, 0, None, None, 0, None) == 1
+    assert lib.kvq_append_quantize(None, 0, None, None, None) == 1
+    assert lib.kvq_decode_attention(None, 0, None, 1, 1.0, None, 0, None, 0, None) == 1
+    n = ctypes.c_int32()
+    assert lib.kvq_cache_length(None, 0, ctypes.byref(n)) == 1
+    assert lib.kvq_cache_status(None, None, None) == 1

@@ -1,0 +1,170 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded fp16 inputs, at sizes the oracle finishes in seconds that still
+span several tiles and a ragged tail. Codes, scales, zero points, outlier
+lists and the fp16 key residual must be bit-exact; attention must be within
+1e-3 (per-row max relative error) of the fp64 oracle on the same dequantized
+cache."""
+import math
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+from bit_quantized_kv_kvq_gb300 import workloads as W
+from bit_quantized_kv_kvq_gb300.synth import LayerSource
+from oracle import kvq_oracle as O
+from tests import kvq_check as K
+
+pytestmark = pytest.mark.gpu
+
+# Small versions of the five workloads: same codec and distribution, fewer
+# streams, lengths with a ragged last tile / residual.
+SMALL = [
+    ("tiny_q8", replace(W.TINY_Q8, seq_len=1000), 70),
+    ("tiny_q8_full", W.TINY_Q8, 3),
+    ("llama7b", replace(W.LLAMA7B_16K, batch=2, num_q_heads=4, num_kv_heads=4, seq_len=357), 30),
+    ("llama70b", replace(W.LLAMA70B_32K, batch=1, num_q_heads=16, num_kv_heads=2, seq_len=461), 60),
+    ("dense_sparse", replace(W.DENSE_SPARSE_128K, num_q_heads=4, num_kv_heads=4, seq_len=269), 60),
+    ("llama8b", replace(W.LLAMA8B_FULL, num_layers=2, num_q_heads=8, num_kv_heads=2, seq_len=242), 20),
+]
+
+
+def _run_case(wl, appends, check_every=7, layer=None):
+    torch.manual_seed(0)
+    layers = list(range(wl.num_layers)) if layer is None else [layer]
+    cache = K.make_gpu_cache(wl, wl.seq_len + appends + 5)
+    scale = 1.0 / math.sqrt(wl.head_dim)
+    worst = 0.0
+    for li in layers:
+        src = LayerSource(wl, li, device="cpu")
+        k, v = src.kv(wl.seq_len)
+        oc = O.OracleCache(K.spec_of(wl), wl.batch * wl.num_kv_heads)
+        oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+        cache.prefill(li, k.cuda(), v.cuda())
+        torch.cuda.synchronize()
+        for n in range(wl.batch * wl.num_kv_heads):
+            K.assert_state_equal(K.gpu_state(cache, li, n), K.oracle_state(oc, n), "prefill n=%d" % n)
+        for step in range(appends + 1):
+            if step > 0:
+                _, k1, v1 = src.step(step)
+                oc.append(K.streams_of(k1, wl), K.streams_of(v1, wl))
+                cache.append(li, k1.cuda(), v1.cuda())
+            if step % check_every == 0 or step == appends:
+                q, _, _ = src.step(10_000 + step)
+                o = cache.decode(li, q.cuda(), scale)
+                ref = oc.decode(K.q_streams(q, wl), scale)
+                got = o.cpu().double().reshape(ref.shape).numpy()
+                worst = max(worst, K.assert_attention_close(got, ref, where="step %d" % step))
+        torch.cuda.synchronize()
+        for n in range(wl.batch * wl.num_kv_heads):
+            K.assert_state_equal(K.gpu_state(cache, li, n), K.oracle_state(oc, n),
+                                 "after %d appends n=%d" % (appends, n))
+    assert cache.status() == 0
+    return worst
+
+
+@pytest.mark.parametrize("name,wl,appends", SMALL, ids=[s[0] for s in SMALL])
+def test_parity_small(name, wl, appends):
+    _run_case(wl, appends)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 0])
+def test_split_count_invariance(splits):
+    wl = replace(W.LLAMA70B_32K, batch=1, num_q_heads=16, num_kv_heads=2, seq_len=1000)
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(wl.seq_len)
+    q, _, _ = src.step(1)
+    cache = K.make_gpu_cache(wl, wl.seq_len)
+    cache.prefill(0, k.cuda(), v.cuda())
+    oc = O.OracleCache(K.spec_of(wl), wl.batch * wl.num_kv_heads)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    ref = oc.decode(K.q_streams(q, wl), 0.088)
+    cache.set_decode_splits(splits)
+    o = cache.decode(0, q.cuda(), 0.088).cpu().double().reshape(ref.shape).numpy()
+    K.assert_attention_close(o, ref)
+
+
+@pytest.mark.parametrize("seq", [1, 2, 63, 64, 65, 127, 128, 129])
+@pytest.mark.parametrize("kmode", [W.ASYM_PER_CHANNEL, W.ASYM_PER_TOKEN])
+def test_short_and_boundary_lengths(seq, kmode):
+    wl = replace(W.DENSE_SPARSE_128K, num_q_heads=4, num_kv_heads=2, seq_len=seq, k_mode=kmode,
+                 k_group=64 if kmode == W.ASYM_PER_CHANNEL else 32)
+    _run_case(wl, appends=3, check_every=1)
+
+
+@pytest.mark.parametrize("bits", [3, 4, 8])
+@pytest.mark.parametrize("gqa", [1, 2, 4, 8])
+def test_codec_and_gqa_grid(bits, gqa):
+    wl = replace(W.LLAMA7B_16K, batch=1, num_kv_heads=2, num_q_heads=2 * gqa, seq_len=200,
+                 k_bits=bits, v_bits=bits, k_group=128 if bits == 3 else 64,
+                 v_group=128 if bits == 3 else 32)
+    _run_case(wl, appends=2, check_every=1)
+
+
+def test_sym_group16_and_fp16_output():
+    wl = replace(W.TINY_Q8, seq_len=300, k_group=16, v_group=16)
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(wl.seq_len)
+    q, _, _ = src.step(0)
+    cache = K.make_gpu_cache(wl, 400)
+    cache.prefill(0, k.cuda(), v.cuda())
+    oc = O.OracleCache(K.spec_of(wl), wl.batch * wl.num_kv_heads)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    torch.cuda.synchronize()
+    for n in range(2):
+        K.assert_state_equal(K.gpu_state(cache, 0, n), K.oracle_state(oc, n))
+    o16 = cache.decode(0, q.cuda(), 0.1, out_dtype=torch.float16)
+    ref = oc.decode(K.q_streams(q, wl), 0.1)
+    K.assert_attention_close(o16.cpu().double().reshape(ref.shape).numpy(), ref, tol=2e-3)
+
+
+def test_degenerate_groups_on_gpu():
+    """Constant rows, all-zero rows and a row of equal magnitudes (outlier
+    ties) quantize exactly as the oracle does."""
+    wl = replace(W.DENSE_SPARSE_128K, num_q_heads=2, num_kv_heads=2, seq_len=130)
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(wl.seq_len)
+    k[0, 0, :64] = 1.5          # a whole constant key block
+    v[0, 0, 3] = 0.0            # an all-zero value row
+    v[0, 1, 5] = -2.0           # every entry ties in magnitude
+    v[0, 1, 5, ::2] = 2.0
+    k[0, 1, 70, :] = 0.0
+    cache = K.make_gpu_cache(wl, 200)
+    cache.prefill(0, k.cuda(), v.cuda())
+    oc = O.OracleCache(K.spec_of(wl), 2)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    torch.cuda.synchronize()
+    for n in range(2):
+        K.assert_state_equal(K.gpu_state(cache, 0, n), K.oracle_state(oc, n))
+    q, _, _ = src.step(0)
+    o = cache.decode(0, q.cuda(), 0.09).cpu().double().reshape(2, 1, 128).numpy()
+    K.assert_attention_close(o, oc.decode(K.q_streams(q, wl), 0.09))
+
+
+def test_errors_are_reported_not_raised_on_device():
+    import bit_quantized_kv_kvq_gb300 as kvq
+    wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=2, num_kv_heads=2, seq_len=10)
+    cache = K.make_gpu_cache(wl, 11)
+    q = torch.zeros((1, 2, 128), dtype=torch.float16, device="cuda")
+    with pytest.raises(kvq.KVQError) as e:
+        cache.decode(0, q, 1.0)          # empty layer
+    assert e.value.status == 1
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(11)
+    with pytest.raises(kvq.KVQError) as e:
+        cache.prefill(0, torch.cat([k, k], 2).cuda(), torch.cat([v, v], 2).cuda())
+    assert e.value.status == 4
+    cache.prefill(0, k.cuda(), v.cuda())
+    _, k1, v1 = src.step(1)
+    with pytest.raises(kvq.KVQError) as e:
+        cache.append(0, k1.cuda(), v1.cuda())   # full
+    assert e.value.status == 4
+    with pytest.raises(kvq.KVQError) as e:
+        cache.decode(0, torch.zeros((1, 3, 128), dtype=torch.float16, device="cuda"), 1.0)
+    assert e.value.status == 1
+    ws = torch.empty(16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(kvq.KVQError) as e:
+        cache.decode(0, q, 1.0, workspace=ws)
+    assert e.value.status == 3
+    assert cache.status() == 0

@@ -453,3 +453,9 @@ def test_packed_bytes_by_hand():
     got = O.packed_cache_bytes(1, 4, 8, 128, 32768, 3, 3, O.ASYM_PER_CHANNEL,
                                O.ASYM_PER_TOKEN, 128, 128)
     assert got == 4 * 8 * 32768 * 2 * (52 + 4)
+
+
+def test_zero_minimum_is_positive_zero():
+    x = np.array([[-0.0, 0.0, 1.0, 2.0]], np.float16)
+    _, s16, z16 = O.quantize_asym(x, 4)
+    assert z16.view(np.uint16)[0] == 0
