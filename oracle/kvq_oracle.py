@@ -166,8 +166,10 @@ def quantize_asym(x16, bits, mask=None):
     mx = np.where(live, x, np.float32(-np.inf)).max(axis=-1)
     mn = np.where(any_live, mn, np.float32(0))
     mx = np.where(any_live, mx, np.float32(0))
-    # reading R15: a zero minimum is stored as +0 (-0 + +0 = +0 under RNE)
+    # reading R15: zero extremes are taken as +0 (-0 + +0 = +0 under RNE), so
+    # the stored zero point and scale never carry a negative zero
     mn = mn + np.float32(0)
+    mx = mx + np.float32(0)
     levels = np.float32(2 ** bits - 1)
     s32 = (mx - mn) / levels
     s16 = s32.astype(np.float16)

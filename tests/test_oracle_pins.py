@@ -455,7 +455,10 @@ def test_packed_bytes_by_hand():
     assert got == 4 * 8 * 32768 * 2 * (52 + 4)
 
 
-def test_zero_minimum_is_positive_zero():
+def test_zero_extremes_are_positive_zero():
     x = np.array([[-0.0, 0.0, 1.0, 2.0]], np.float16)
     _, s16, z16 = O.quantize_asym(x, 4)
     assert z16.view(np.uint16)[0] == 0
+    x = np.array([[-0.0, -0.0, -0.0, -0.0], [0.0, -0.0, 0.0, -0.0]], np.float16)
+    _, s16, z16 = O.quantize_asym(x, 4)
+    assert np.all(s16.view(np.uint16) == 0) and np.all(z16.view(np.uint16) == 0)
