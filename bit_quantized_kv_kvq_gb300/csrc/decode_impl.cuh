@@ -414,6 +414,9 @@ cudaError_t launch_decode_t(const LayerDev& L, const DecodeArgs& a, cudaStream_t
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
+  if (a.occupancy_out)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        a.occupancy_out, decode_split_kernel<KB, KMODE, VB, VMODE, G>, kDecThreads, sm);
   dim3 grid(a.splits, L.n_streams);
   decode_split_kernel<KB, KMODE, VB, VMODE, G><<<grid, kDecThreads, sm, st>>>(L, a);
   return cudaGetLastError();

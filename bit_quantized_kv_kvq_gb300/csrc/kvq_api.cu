@@ -202,22 +202,40 @@ int k_quant_len(const kvq_config& c, int len) {
   return len / c.k_group * c.k_group;
 }
 
-// Splits: enough CTAs for about two waves of 4 CTAs per SM, at least one
-// 64-token tile per split.
-void plan_splits(const kvq_cache* h, int len, int* splits, int* tiles_per_split) {
+// Splits of the sequence: every (stream, split) is one CTA of equal work.
+// With `slots` CTAs resident on the GPU at once, the time of a launch is
+// about waves * (rows per CTA + fixed cost), waves = ceil(CTAs / slots); the
+// split count minimizing it balances wave quantization against short CTAs.
+void plan_splits(const kvq_cache* h, int len, int slots, int* splits, int* tiles_per_split) {
   const int ntiles = (len + kvq::kTile - 1) / kvq::kTile;
-  int want;
   if (h->splits_override > 0) {
-    want = h->splits_override;
-  } else {
-    const int64_t target = (int64_t)h->sm_count * 8;
-    want = (int)((target + h->plan.n_streams - 1) / h->plan.n_streams);
+    int want = h->splits_override < ntiles ? h->splits_override : ntiles;
+    int tps = (ntiles + want - 1) / want;
+    *tiles_per_split = tps;
+    *splits = (ntiles + tps - 1) / tps;
+    return;
   }
-  if (want < 1) want = 1;
-  if (want > ntiles) want = ntiles;
-  int tps = (ntiles + want - 1) / want;
-  *tiles_per_split = tps;
-  *splits = (ntiles + tps - 1) / tps;
+  const int64_t n = h->plan.n_streams;
+  if (slots < 1) slots = 1;
+  const double fixed_rows = 192.0;  // pipeline fill, query load and merge, in rows
+  double best = 1e300;
+  int best_s = 1, best_tps = ntiles;
+  const int s_max = ntiles < 4096 ? ntiles : 4096;
+  for (int s = 1; s <= s_max; ++s) {
+    const int tps = (ntiles + s - 1) / s;
+    const int s2 = (ntiles + tps - 1) / tps;
+    if (s2 != s) continue;  // same shape as a smaller s
+    const int64_t ctas = n * s2;
+    const int64_t waves = (ctas + slots - 1) / slots;
+    const double t = (double)waves * ((double)tps * kvq::kTile + fixed_rows);
+    if (t < best * 0.999) {
+      best = t;
+      best_s = s2;
+      best_tps = tps;
+    }
+  }
+  *splits = best_s;
+  *tiles_per_split = best_tps;
 }
 
 size_t workspace_for(const kvq_cache* h, int num_q_heads, int splits) {
@@ -351,12 +369,20 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
   if (!kvq::decode_supported(L, gqa))
     return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for this codec pair with %d query heads per kv-head",
                 gqa);
+  kvq::DecodeArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.gqa = gqa;
+  a.num_q_heads = num_q_heads;
+  int occ = 0;
+  a.occupancy_out = &occ;
+  cudaError_t e = kvq::launch_decode(L, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "decode occupancy query");
+  a.occupancy_out = nullptr;
   int splits = 1, tps = 1;
-  plan_splits(h, len, &splits, &tps);
+  plan_splits(h, len, h->sm_count * (occ > 0 ? occ : 1), &splits, &tps);
   const size_t need = workspace_for(h, num_q_heads, splits);
   if (ws_bytes < need)
     return fail(KVQ_ERR_BUFFER_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, need);
-  kvq::DecodeArgs a;
   a.q = static_cast<const __half*>(q);
   a.out = out;
   a.out_dtype = out_dtype;
@@ -370,7 +396,7 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
   const int64_t rows = (int64_t)h->cfg.batch * num_q_heads;
   a.part_o = static_cast<float*>(workspace);
   a.part_ml = a.part_o + rows * splits * kvq::kHeadDim;
-  cudaError_t e = kvq::launch_decode(L, a, static_cast<cudaStream_t>(stream));
+  e = kvq::launch_decode(L, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return KVQ_OK;
 }

@@ -68,10 +68,15 @@ struct DecodeArgs {
   int tiles_per_split;
   float* part_o;        // [B*Hq][splits][D]
   float* part_ml;       // [B*Hq][splits][2]
+  int* occupancy_out;   // non-null: report resident CTAs per SM of the kernel, launch nothing
 };
 
 cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);
 
 bool decode_supported(const LayerDev& L, int gqa);
+bool decode_mha_supported(const LayerDev& L);
+cudaError_t launch_decode_mha(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);
+bool decode_gqa_supported(const LayerDev& L, int gqa);
+cudaError_t launch_decode_gqa(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);
 
 }  // namespace kvq

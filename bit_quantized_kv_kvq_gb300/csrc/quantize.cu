@@ -1,4 +1,5 @@
-// Quantize kernels: prefill (whole prompt) and append (one token per stream).
+// Append quantize: one new token per stream (the prefill kernel is in
+// prefill_impl.cuh).
 //
 // Codec (pages cited by short name, address and section):
 //  - asymmetric min/max groups, offset = group minimum, codes clamped to
@@ -157,7 +158,8 @@ __device__ void quant_row_warp(const __half* __restrict__ src, const TensorDev& 
       mn = 0.0f;
       mx = 0.0f;
     }
-    mn = __fadd_rn(mn, 0.0f);  // a zero minimum is stored as +0
+    mn = __fadd_rn(mn, 0.0f);  // zero extremes are taken as +0
+    mx = __fadd_rn(mx, 0.0f);
     s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)levels));
     z16 = __float2half_rn(mn);
     const float s = __half2float(s16);
@@ -287,6 +289,7 @@ __device__ void quant_kblock(const BlockSmem& sm, int T, int t0, int blk, const 
       mx = 0.0f;
     }
     mn = __fadd_rn(mn, 0.0f);
+    mx = __fadd_rn(mx, 0.0f);
     __half s16 = __float2half_rn(__fdiv_rn(__fsub_rn(mx, mn), (float)levels));
     __half z16 = __float2half_rn(mn);
     reinterpret_cast<__half2*>(K.meta + (int64_t)n * K.meta_sstride)[(int64_t)blk * kHeadDim + c] =
@@ -324,49 +327,6 @@ __device__ void quant_kblock(const BlockSmem& sm, int T, int t0, int blk, const 
 // ---------------------------------------------------------------------------
 // Kernels
 // ---------------------------------------------------------------------------
-constexpr int kRowThreads = 256;
-
-template <int BITS, bool SYM>
-__global__ void __launch_bounds__(kRowThreads)
-    quant_rows_kernel(TensorDev T, const __half* __restrict__ src, int seq_len, int n_streams,
-                      int kout) {
-  __shared__ __align__(16) uint8_t scratch[kRowThreads / 32][kHeadDim];
-  const int lane = threadIdx.x & 31;
-  const int wib = threadIdx.x >> 5;
-  const int64_t total = (int64_t)n_streams * seq_len;
-  const int64_t nwarps = (int64_t)gridDim.x * (kRowThreads / 32);
-  for (int64_t r = (int64_t)blockIdx.x * (kRowThreads / 32) + wib; r < total; r += nwarps) {
-    const int n = (int)(r / seq_len);
-    const int t = (int)(r - (int64_t)n * seq_len);
-    quant_row_warp<BITS, SYM>(src + r * kHeadDim, T, n, t, kout, lane, scratch[wib]);
-  }
-}
-
-template <int BITS>
-__global__ void __launch_bounds__(256)
-    kblock_prefill_kernel(TensorDev K, const __half* __restrict__ src, int seq_len,
-                          int n_full_blocks, int resid, int kout) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  const int T = K.group;
-  const int n = blockIdx.y;
-  const int blk = blockIdx.x;
-  const __half* srcn = src + (int64_t)n * seq_len * kHeadDim;
-  if (blk < n_full_blocks) {
-    BlockSmem sm = carve_block_smem(smem_raw, T);
-    const int t0 = blk * T;
-    const uint4* s4 = reinterpret_cast<const uint4*>(srcn + (int64_t)t0 * kHeadDim);
-    uint4* d4 = reinterpret_cast<uint4*>(sm.tile);
-    for (int i = threadIdx.x; i < T * (kHeadDim / 8); i += blockDim.x) d4[i] = s4[i];
-    __syncthreads();
-    quant_kblock<BITS>(sm, T, t0, blk, K, n, kout);
-  } else {
-    const int t0 = n_full_blocks * T;
-    const uint4* s4 = reinterpret_cast<const uint4*>(srcn + (int64_t)t0 * kHeadDim);
-    uint4* d4 = reinterpret_cast<uint4*>(K.resid + (int64_t)n * K.resid_sstride);
-    for (int i = threadIdx.x; i < resid * (kHeadDim / 8); i += blockDim.x) d4[i] = s4[i];
-  }
-}
-
 template <int KB, int KMODE, int VB, bool VSYM>
 __global__ void __launch_bounds__(256)
     append_kernel(LayerDev L, const __half* __restrict__ k1, const __half* __restrict__ v1,
@@ -409,60 +369,10 @@ __global__ void __launch_bounds__(256)
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
-int g_sm_count = 0;
-
-int sm_count() {
-  if (g_sm_count == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sm_count, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sm_count <= 0) g_sm_count = 1;
-  }
-  return g_sm_count;
-}
-
-template <int BITS, bool SYM>
-cudaError_t launch_rows_t(const TensorDev& T, const __half* src, int seq_len, int n_streams,
-                          int kout, cudaStream_t st) {
-  const int64_t rows = (int64_t)n_streams * seq_len;
-  int64_t want = (rows + (kRowThreads / 32) - 1) / (kRowThreads / 32);
-  int64_t cap = (int64_t)sm_count() * 8;
-  int grid = (int)(want < cap ? want : cap);
-  if (grid < 1) grid = 1;
-  quant_rows_kernel<BITS, SYM><<<grid, kRowThreads, 0, st>>>(T, src, seq_len, n_streams, kout);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_rows(const TensorDev& T, const __half* src, int seq_len, int n_streams,
-                        int kout, cudaStream_t st) {
-  if (T.mode == KVQ_SYM_PER_TOKEN) return launch_rows_t<8, true>(T, src, seq_len, n_streams, kout, st);
-  switch (T.bits) {
-    case 3: return launch_rows_t<3, false>(T, src, seq_len, n_streams, kout, st);
-    case 4: return launch_rows_t<4, false>(T, src, seq_len, n_streams, kout, st);
-    default: return launch_rows_t<8, false>(T, src, seq_len, n_streams, kout, st);
-  }
-}
-
 template <typename F>
 cudaError_t ensure_smem(F* kernel, size_t bytes) {
   if (bytes <= 48 * 1024) return cudaSuccess;
   return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
-template <int BITS>
-cudaError_t launch_kblocks_t(const TensorDev& K, const __half* src, int seq_len, int n_streams,
-                             int kout, cudaStream_t st) {
-  const int T = K.group;
-  const int nfull = seq_len / T;
-  const int resid = seq_len - nfull * T;
-  const int gx = nfull + (resid > 0 ? 1 : 0);
-  if (gx == 0) return cudaSuccess;
-  const size_t sm = block_smem_bytes(T);
-  cudaError_t e = ensure_smem(kblock_prefill_kernel<BITS>, sm);
-  if (e != cudaSuccess) return e;
-  dim3 grid(gx, n_streams);
-  kblock_prefill_kernel<BITS><<<grid, 256, sm, st>>>(K, src, seq_len, nfull, resid, kout);
-  return cudaGetLastError();
 }
 
 template <int KB, int KMODE, int VB, bool VSYM>
@@ -489,19 +399,6 @@ cudaError_t launch_append_v(const LayerDev& L, const __half* k1, const __half* v
 }
 
 }  // namespace
-
-cudaError_t launch_prefill(const LayerDev& L, const __half* k, const __half* v, int seq_len,
-                           cudaStream_t st) {
-  if (seq_len <= 0) return cudaSuccess;
-  cudaError_t e = launch_rows(L.v, v, seq_len, L.n_streams, L.outliers, st);
-  if (e != cudaSuccess) return e;
-  if (L.k.mode != KVQ_ASYM_PER_CHANNEL) return launch_rows(L.k, k, seq_len, L.n_streams, L.outliers, st);
-  switch (L.k.bits) {
-    case 3: return launch_kblocks_t<3>(L.k, k, seq_len, L.n_streams, L.outliers, st);
-    case 4: return launch_kblocks_t<4>(L.k, k, seq_len, L.n_streams, L.outliers, st);
-    default: return launch_kblocks_t<8>(L.k, k, seq_len, L.n_streams, L.outliers, st);
-  }
-}
 
 cudaError_t launch_append(const LayerDev& L, const __half* k1, const __half* v1, int pos,
                           cudaStream_t st) {
