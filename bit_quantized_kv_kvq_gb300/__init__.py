@@ -69,6 +69,7 @@ _SIGNATURES = {
     "kvq_append_quantize": [_P, _I, _P, _P, _P],
     "kvq_decode_workspace_bytes": [_P, _I, ctypes.POINTER(ctypes.c_size_t)],
     "kvq_decode_attention": [_P, _I, _P, _I, ctypes.c_float, _P, _I, _P, ctypes.c_size_t, _P],
+    "kvq_decode_attention_static": [_P, _I, _P, _I, ctypes.c_float, _P, _I, _P],
     "kvq_cache_set_decode_splits": [_P, _I],
     "kvq_cache_get_layout": [_P, _I, ctypes.POINTER(Layout)],
     "kvq_cache_length": [_P, _I, ctypes.POINTER(_I)],
@@ -189,6 +190,22 @@ class QuantizedKVCache:
                                          float(softmax_scale), ctypes.c_void_p(out.data_ptr()),
                                          code, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
                                          _stream_ptr(stream)))
+        return out
+
+    def decode_static(self, layer, q, softmax_scale, out=None, out_dtype=torch.float32,
+                      stream=None):
+        """decode() without a workspace: the split scratch is the library's own
+        device array (for callers that cannot allocate; see kvq.h)."""
+        c = self.cfg
+        hq = q.shape[1]
+        _check_half(q, (c.batch, hq, c.head_dim), "q")
+        if out is None:
+            out = torch.empty((c.batch, hq, c.head_dim), dtype=out_dtype, device=q.device)
+        code = {torch.float32: F32, torch.float16: F16}[out.dtype]
+        check(lib().kvq_decode_attention_static(self.handle, layer, ctypes.c_void_p(q.data_ptr()),
+                                                hq, float(softmax_scale),
+                                                ctypes.c_void_p(out.data_ptr()), code,
+                                                _stream_ptr(stream)))
         return out
 
     # -- inspection ---------------------------------------------------------

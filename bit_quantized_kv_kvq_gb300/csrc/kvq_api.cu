@@ -252,6 +252,10 @@ kvq_status check_layer(const kvq_cache* h, int layer) {
 
 }  // namespace
 
+namespace kvq {
+void set_error_message(const char* msg) { g_err = msg ? msg : ""; }
+}  // namespace kvq
+
 extern "C" {
 
 kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes) {

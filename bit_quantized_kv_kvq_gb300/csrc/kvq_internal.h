@@ -79,4 +79,7 @@ cudaError_t launch_decode_mha(const LayerDev& L, const DecodeArgs& a, cudaStream
 bool decode_gqa_supported(const LayerDev& L, int gqa);
 cudaError_t launch_decode_gqa(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);
 
+// Replaces the thread-local message returned by kvq_last_error().
+void set_error_message(const char* msg);
+
 }  // namespace kvq

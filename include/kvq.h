@@ -196,6 +196,26 @@ KVQ_API kvq_status kvq_decode_attention(kvq_cache* cache, int32_t layer, const v
                                 int32_t out_dtype, void* workspace, size_t ws_bytes,
                                 void* stream);
 
+/* Decode attention exactly as kvq_decode_attention, but with no workspace
+ * argument: for callers that cannot allocate device memory (host callbacks
+ * and other code that may not call the CUDA allocator, plugins whose host
+ * program owns every allocation, servers that forbid allocating after
+ * start-up). The pages describe no counterpart of this call; it exists for
+ * those callers only.
+ * Scratch: the split partials go to a device array the library declares
+ * itself, 4 MiB on every GPU that loads the library, kept until the process
+ * exits. A call that would need more returns KVQ_ERR_BUFFER_TOO_SMALL (use
+ * kvq_decode_attention with a workspace then). The first call on a device
+ * looks up that array's address with the device current, so make that first
+ * call before any stream capture. All calls share the one array and each
+ * call overwrites it completely before reading it (nothing needs clearing);
+ * calls that overlap on the GPU (several streams, or another thread) race on
+ * it. q, out, num_q_heads, softmax_scale and out_dtype as in
+ * kvq_decode_attention; the cache's device must be current. */
+KVQ_API kvq_status kvq_decode_attention_static(kvq_cache* cache, int32_t layer, const void* q,
+                                               int32_t num_q_heads, float softmax_scale,
+                                               void* out, int32_t out_dtype, void* stream);
+
 /* Forces the number of sequence splits of later decode calls (0 = automatic).
  * Results agree for every split count up to rounding; used by tests. */
 KVQ_API kvq_status kvq_cache_set_decode_splits(kvq_cache* cache, int32_t splits);
