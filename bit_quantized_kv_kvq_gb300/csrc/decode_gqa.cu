@@ -8,7 +8,7 @@ bool decode_gqa_supported(const LayerDev& L, int gqa) {
   const TensorDev& k = L.k;
   const TensorDev& v = L.v;
   if (L.outliers > 0) return false;
-  if (k.bits == 3 || v.bits == 3) return false;
+  if ((k.bits == 3) != (v.bits == 3)) return false;  // 3-bit keys and values go together
   if (v.mode == KVQ_ASYM_PER_CHANNEL || v.group < 32) return false;
   if (k.mode != KVQ_ASYM_PER_CHANNEL && k.group < 32) return false;
   if ((k.mode == KVQ_SYM_PER_TOKEN) != (v.mode == KVQ_SYM_PER_TOKEN)) return false;
@@ -23,6 +23,10 @@ cudaError_t launch_decode_gqa(const LayerDev& L, const DecodeArgs& a, cudaStream
   if (kb == KB_ && km == KM_) {                                                    \
     if (vb == 4) return gqa::launch_t<KB_, KM_, 4, KVQ_ASYM_PER_TOKEN>(L, a, st);  \
     return gqa::launch_t<KB_, KM_, 8, KVQ_ASYM_PER_TOKEN>(L, a, st);               \
+  }
+  if (kb == 3 && vb == 3) {
+    if (km == KVQ_ASYM_PER_CHANNEL) return gqa::launch_t<3, KVQ_ASYM_PER_CHANNEL, 3, KVQ_ASYM_PER_TOKEN>(L, a, st);
+    return gqa::launch_t<3, KVQ_ASYM_PER_TOKEN, 3, KVQ_ASYM_PER_TOKEN>(L, a, st);
   }
   KVQ_GQA(4, KVQ_ASYM_PER_CHANNEL)
   KVQ_GQA(8, KVQ_ASYM_PER_CHANNEL)

@@ -27,7 +27,6 @@ namespace gqa {
 constexpr int kWarps = 4;
 constexpr int kThreads = 32 * kWarps;
 constexpr int kRows = 32;  // tokens per warp tile (two m16 tiles)
-constexpr int kStagesPerWarp = 2;
 constexpr float kLazy = 8.0f;
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -56,9 +55,18 @@ __device__ __forceinline__ void split2(float v, __half& hi, __half& lo) {
   lo = __float2half_rn(v - __half2float(hi));
 }
 
+__device__ __forceinline__ uint32_t hfma2u(uint32_t x, uint32_t y, uint32_t z) {
+  __half2 r = __hfma2(*reinterpret_cast<__half2*>(&x), *reinterpret_cast<__half2*>(&y),
+                      *reinterpret_cast<__half2*>(&z));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
 // fp16 code pair (1024 + n) in the two halves -> exact (n, n').
 constexpr uint32_t kH1024 = 0x64006400u;  // (1024, 1024)
 constexpr uint32_t kH1152 = 0x64806480u;  // (1152, 1152): offset-binary int8
+// (1024 + n, 1024 + 4 n') * (1, 1/4) + (-1024, -256) = (n, n') exactly
+constexpr uint32_t kH1Quarter = 0x34003C00u;     // (1.0, 0.25)
+constexpr uint32_t kHNeg1024_256 = 0xDC00E400u;  // (-1024, -256)
 
 template <int KB, int KMODE, int VB, int VMODE>
 struct Cfg {
@@ -70,12 +78,13 @@ struct Cfg {
   static constexpr int VC_BYTES = kRows * VW * 4;
   static constexpr int META = 512;
   static constexpr int STAGE = KC_BYTES + VC_BYTES + 2 * META;
+  static constexpr int kStagesPerWarp = STAGE <= 5 * 1024 ? 3 : 2;
   static constexpr size_t stage_bytes() { return (size_t)kWarps * kStagesPerWarp * STAGE; }
   static constexpr size_t merge_bytes() { return (size_t)kWarps * 8 * kHeadDim * 4; }
   static constexpr size_t smem_bytes() {
     return (stage_bytes() > merge_bytes() ? stage_bytes() : merge_bytes()) +
            8 * kHeadDim * 4 /*q*/ + kWarps * 8 * 2 * 4 /*m, l*/ +
-           kWarps * kStagesPerWarp * 8 /*bars*/;
+           kWarps * 3 * 8 /*bars*/;
   }
 };
 
@@ -84,8 +93,26 @@ struct Cfg {
 // 2t4+8 <-> 2t4+1, 2t4+9 <-> 9+2t4 (offsets inside the chunk).
 // 8-bit keys: chunk kc (group q, local l) uses word q*(Gp/4) + t4*(Gp/16) + l;
 // slots 2t4, 2t4+1, 2t4+8, 2t4+9 <-> bytes 0, 2, 1, 3 of that word.
+// 3-bit keys (ten codes per word, thirteen words per row): a thread with t4
+// reads words t4, t4+4, t4+8 and the last word; its 16 code pairs are
+//   p = 0..11: codes (j, j+6) of word t4 + 4*(p/4), j = p mod 4,
+//   p = 12, 13: code 4 / code 5 of words t4 and t4+4,
+//   p = 14, 15: code 4 / code 5 of word t4+8 with codes 2t4 / 2t4+1 of word 12;
+// chunk kc uses pairs 2kc (slots 2t4, 2t4+1) and 2kc+1 (slots 2t4+8, 2t4+9).
+__device__ __forceinline__ int key3_pair_channel(int p, int t4, int second) {
+  if (p < 12) {
+    const int w = t4 + 4 * (p >> 2), j = p & 3;
+    return 10 * w + j + (second ? 6 : 0);
+  }
+  if (p == 12) return second ? 10 * (t4 + 4) + 4 : 10 * t4 + 4;
+  if (p == 13) return second ? 10 * (t4 + 4) + 5 : 10 * t4 + 5;
+  if (p == 14) return second ? 120 + 2 * t4 : 10 * (t4 + 8) + 4;
+  return second ? 121 + 2 * t4 : 10 * (t4 + 8) + 5;
+}
+
 template <int KB>
 __device__ __forceinline__ int key_channel(int kc, int t4, int which, int gp) {
+  if (KB == 3) return key3_pair_channel(2 * kc + (which >> 1), t4, which & 1);
   if (KB == 4) {
     const int base = 16 * kc;
     return which == 0 ? base + 2 * t4 : which == 1 ? base + 8 + 2 * t4
@@ -99,9 +126,10 @@ __device__ __forceinline__ int key_channel(int kc, int t4, int which, int gp) {
 }
 
 template <int KB, int KMODE, int VB, int VMODE>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     decode_gqa_kernel(LayerDev L, DecodeArgs a) {
   using C = Cfg<KB, KMODE, VB, VMODE>;
+  constexpr int kStagesPerWarp = C::kStagesPerWarp;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
@@ -129,6 +157,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int kgpr = C::KCH ? 1 : kHeadDim / Gk;
   const int vgpr = kHeadDim / Gv;
   const int gp = C::KCH ? kHeadDim : Gk;  // key group that chunks must not straddle
+  const int mpg = Gv / 16;                 // m16 value-channel tiles per value group (2, 4, 8)
+  const int mpg_log2 = mpg == 8 ? 3 : mpg == 4 ? 2 : 1;
 
   const uint32_t* kcodes = L.k.codes + (int64_t)n * L.k.codes_sstride;
   const uint32_t* vcodes = L.v.codes + (int64_t)n * L.v.codes_sstride;
@@ -262,7 +292,31 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int kc = 0; kc < 8; ++kc) {
           uint32_t af[4];
-          if (KB == 4) {
+          if (KB == 3) {
+            // rows r0 / r1: pairs 2kc (-> a0 / a1) and 2kc+1 (-> a2 / a3)
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+              const uint32_t* rw = kc_s + (half ? r1 : r0) * C::KW;
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int p = 2 * kc + e;
+                uint32_t v;
+                if (p < 12) {
+                  const uint32_t w = rw[t4 + 4 * (p >> 2)];
+                  v = ((w >> (3 * (p & 3))) & 0x001C0007u) | kH1024;
+                  v = hfma2u(v, kH1Quarter, kHNeg1024_256);  // (n_j, n_{j+6})
+                } else {
+                  uint32_t lo, hi;
+                  if (p == 12) { lo = rw[t4] >> 12; hi = rw[t4 + 4] >> 12; }
+                  else if (p == 13) { lo = rw[t4] >> 15; hi = rw[t4 + 4] >> 15; }
+                  else if (p == 14) { lo = rw[t4 + 8] >> 12; hi = rw[12] >> (6 * t4); }
+                  else { lo = rw[t4 + 8] >> 15; hi = rw[12] >> (6 * t4 + 3); }
+                  v = hsub2u((__byte_perm(lo, hi, 0x5410u) & 0x00070007u) | kH1024, kH1024);
+                }
+                af[2 * e + half] = v;
+              }
+            }
+          } else if (KB == 4) {
             const uint2 w0 = *reinterpret_cast<const uint2*>(kc_s + r0 * C::KW + 2 * kc);
             const uint2 w1 = *reinterpret_cast<const uint2*>(kc_s + r1 * C::KW + 2 * kc);
             const uint32_t sel = (uint32_t)(t4 | (t4 << 4) | ((4 + t4) << 8) | ((4 + t4) << 12));
@@ -419,7 +473,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ---- PV: per 16-token step; B operand (P' = p * s_t) per value group ---------
-    const int mpg = Gv / 16;  // m16 channel tiles per value group
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
       const int r0 = 16 * ks + g, r1 = r0 + 8;  // rows this thread holds in C layout
@@ -458,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
 #pragma unroll
       for (int mv = 0; mv < 8; ++mv) {
-        const int q = mv / mpg, l = mv - q * mpg;
+        const int q = mv >> mpg_log2, l = mv & (mpg - 1);
         uint32_t b0h = bph0[0], b1h = bph1[0], b0l = bpl0[0], b1l = bpl1[0];
 #pragma unroll
         for (int qq = 1; qq < 4; ++qq)
@@ -466,7 +519,20 @@ __global__ void __launch_bounds__(kThreads, 2)
             b0h = bph0[qq]; b1h = bph1[qq]; b0l = bpl0[qq]; b1l = bpl1[qq];
           }
         uint32_t af[4];
-        if (VB == 4) {
+        if (VB == 3) {
+          // code pair P = 8 mv + g: word P / 5, codes (2j, 2j+1), j = P mod 5;
+          // P >= 60: codes of the 8-code last word
+          const int P = 8 * mv + g;
+          const int wi = P < 60 ? P / 5 : 12;
+          const int sh = P < 60 ? 6 * (P % 5) : 6 * (P - 60);
+          const uint32_t wa = vc_s[ra * C::VW + wi] >> sh, wb2 = vc_s[(ra + 1) * C::VW + wi] >> sh;
+          const uint32_t wc = vc_s[(ra + 8) * C::VW + wi] >> sh, wd = vc_s[(ra + 9) * C::VW + wi] >> sh;
+          const uint32_t xab = __byte_perm(wa, wb2, 0x5410u), xcd = __byte_perm(wc, wd, 0x5410u);
+          af[0] = hsub2u((xab & 0x00070007u) | kH1024, kH1024);
+          af[1] = hsub2u(((xab >> 3) & 0x00070007u) | kH1024, kH1024);
+          af[2] = hsub2u((xcd & 0x00070007u) | kH1024, kH1024);
+          af[3] = hsub2u(((xcd >> 3) & 0x00070007u) | kH1024, kH1024);
+        } else if (VB == 4) {
           const int u = g >> 2, i = g & 3;
           const int wi = q * (Gv / 8) + u * (Gv / 16) + l;
           const uint32_t wa = vc_s[ra * C::VW + wi], wb2 = vc_s[(ra + 1) * C::VW + wi];
@@ -528,10 +594,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   float* my = mo + warp * 8 * kHeadDim;  // [8 heads][128]
 #pragma unroll
   for (int mv = 0; mv < 8; ++mv) {
-    const int mpg = Gv / 16;
-    const int q = mv / mpg, l = mv - q * mpg;
+    const int q = mv >> mpg_log2, l = mv & (mpg - 1);
     int cg, cg8;
-    if (VB == 4) {
+    if (VB == 3) {
+      const int P = 8 * mv + g;
+      cg = P < 60 ? 10 * (P / 5) + 2 * (P % 5) : 120 + 2 * (P - 60);
+      cg8 = cg + 1;
+    } else if (VB == 4) {
       const int u = g >> 2, i = g & 3;
       const int wi = q * (Gv / 8) + u * (Gv / 16) + l;
       cg = 8 * wi + 2 * i;

@@ -64,7 +64,7 @@ struct Unpack<8> {
   }
 };
 
-template <int KB, int KMODE, int VB, int VMODE>
+template <int KB, int KMODE, int VB, int VMODE, bool OUTL>
 struct Cfg {
   static constexpr bool KCH = KMODE == KVQ_ASYM_PER_CHANNEL;
   static constexpr bool KSYM = KMODE == KVQ_SYM_PER_TOKEN;
@@ -74,7 +74,10 @@ struct Cfg {
   static constexpr int KC_BYTES = kRows * KW * 4;
   static constexpr int VC_BYTES = kRows * VW * 4;
   static constexpr int META = 512;  // per tile, K and V each (groups of >= 32 channels)
-  static constexpr int STAGE = KC_BYTES + VC_BYTES + 2 * META;
+  // outliers: columns and values of the tile's K and V rows (<= 8 per row)
+  static constexpr int OUT_ONE = kRows * kMaxOutliers * 2;
+  static constexpr int OUT_BYTES = OUTL ? 4 * OUT_ONE : 0;
+  static constexpr int STAGE = KC_BYTES + VC_BYTES + 2 * META + OUT_BYTES;
   static constexpr size_t smem_bytes() {
     return (size_t)kWarps * kStagesPerWarp * STAGE + kHeadDim * 4 /*q*/ +
            (size_t)kWarps * kHeadDim * 4 * 2 /*o, ocorr*/ + kWarps * 2 * 4 /*m, l*/ +
@@ -94,10 +97,10 @@ __device__ __forceinline__ void lds_words(const uint32_t* p, uint32_t (&w)[N]) {
   }
 }
 
-template <int KB, int KMODE, int VB, int VMODE>
+template <int KB, int KMODE, int VB, int VMODE, bool OUTL>
 __global__ void __launch_bounds__(kThreads, 4)
     decode_mha_kernel(LayerDev L, DecodeArgs a) {
-  using C = Cfg<KB, KMODE, VB, VMODE>;
+  using C = Cfg<KB, KMODE, VB, VMODE, OUTL>;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int j = lane & 3, r8 = lane >> 2;
@@ -147,7 +150,8 @@ __global__ void __launch_bounds__(kThreads, 4)
     const bool rt = C::KCH && t0 >= kq;
     const uint32_t kmb = C::KCH ? (uint32_t)(kHeadDim * 4) : (uint32_t)(kRows * kgpr * (C::KSYM ? 2 : 4));
     const uint32_t vmb = (uint32_t)(kRows * vgpr * (C::VSYM ? 2 : 4));
-    mbar_arrive_expect_tx(&wb[s], C::VC_BYTES + vmb + (rt ? 0u : C::KC_BYTES + kmb));
+    const uint32_t ob = OUTL ? (uint32_t)(kRows * kout * 2) : 0u;  // one outlier array of the tile
+    mbar_arrive_expect_tx(&wb[s], C::VC_BYTES + vmb + 2 * ob + (rt ? 0u : C::KC_BYTES + kmb + 2 * ob));
     if (!rt) {
       bulk_g2s(base, kcodes + (int64_t)t0 * C::KW, C::KC_BYTES, &wb[s]);
       const unsigned char* ks = C::KCH ? kmeta + (int64_t)(t0 / Gk) * kHeadDim * 4
@@ -157,6 +161,17 @@ __global__ void __launch_bounds__(kThreads, 4)
     bulk_g2s(base + C::KC_BYTES, vcodes + (int64_t)t0 * C::VW, C::VC_BYTES, &wb[s]);
     bulk_g2s(base + C::KC_BYTES + C::VC_BYTES + C::META, vmeta + (int64_t)t0 * vgpr * (C::VSYM ? 2 : 4),
              vmb, &wb[s]);
+    if (OUTL) {
+      // every row holds exactly kout entries, so the tile's entries are contiguous
+      unsigned char* ot = base + C::KC_BYTES + C::VC_BYTES + 2 * C::META;
+      const int64_t e0 = (int64_t)t0 * kout;
+      if (!rt) {
+        bulk_g2s(ot, L.k.col + (int64_t)n * L.k.out_sstride + e0, ob, &wb[s]);
+        bulk_g2s(ot + C::OUT_ONE, L.k.val + (int64_t)n * L.k.out_sstride + e0, ob, &wb[s]);
+      }
+      bulk_g2s(ot + 2 * C::OUT_ONE, L.v.col + (int64_t)n * L.v.out_sstride + e0, ob, &wb[s]);
+      bulk_g2s(ot + 3 * C::OUT_ONE, L.v.val + (int64_t)n * L.v.out_sstride + e0, ob, &wb[s]);
+    }
   };
   if (lane == 0)
     for (int s = 0; s < kStagesPerWarp && s < w_count; ++s) issue(s, s);
@@ -230,15 +245,15 @@ __global__ void __launch_bounds__(kThreads, 4)
         }
         float f[32];
         Unpack<KB>::run(w, f);
-        float d0 = 0.0f, d1 = 0.0f, d2 = 0.0f, d3 = 0.0f;
+        uint64_t dA = 0, dB = 0;  // (0.0f, 0.0f) pairs
 #pragma unroll
         for (int k = 0; k < 32; k += 4) {
-          d0 = fmaf(qq[k], f[k], d0);
-          d1 = fmaf(qq[k + 1], f[k + 1], d1);
-          d2 = fmaf(qq[k + 2], f[k + 2], d2);
-          d3 = fmaf(qq[k + 3], f[k + 3], d3);
+          dA = f2_fma(f2_pack(qq[k], qq[k + 1]), f2_pack(f[k], f[k + 1]), dA);
+          dB = f2_fma(f2_pack(qq[k + 2], qq[k + 3]), f2_pack(f[k + 2], f[k + 3]), dB);
         }
-        float d = (d0 + d1) + (d2 + d3);
+        float a0, a1;
+        f2_unpack(f2_add(dA, dB), a0, a1);
+        float d = a0 + a1;
         if (C::KCH) {
           d += kcorr;
         } else if (C::KSYM) {
@@ -280,27 +295,25 @@ __global__ void __launch_bounds__(kThreads, 4)
     }
 
     // ---- key outliers: e_t += q_c (x - dequant(code 0)) -----------------------
-    if (kout > 0 && !rt) {
+    const uint16_t* ocol = reinterpret_cast<const uint16_t*>(base + C::KC_BYTES + C::VC_BYTES + 2 * C::META);
+    const __half* oval = reinterpret_cast<const __half*>(ocol + C::OUT_ONE / 2);
+    if (OUTL && !rt) {
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
-        const int t = t0 + it * 8 + r8;
+        const int lr = it * 8 + r8;
         float add = 0.0f;
-        if (t < row_end) {
-          const int32_t* rp = L.k.rowptr + (int64_t)n * L.k.rowptr_sstride;
-          const int beg = rp[t], end = rp[t + 1];
-          for (int e = beg + j; e < end; e += 4) {
-            const int64_t ei = (int64_t)n * L.k.out_sstride + e;
-            const int c = L.k.col[ei];
-            const float x = __half2float(L.k.val[ei]);
-            float z0 = 0.0f;
-            if (C::KCH) z0 = __high2float(reinterpret_cast<const __half2*>(km)[c]);
-            else if (!C::KSYM) z0 = __high2float(reinterpret_cast<const __half2*>(km)[(it * 8 + r8) * kgpr + c / Gk]);
-            add = fmaf(qf[c], x - z0, add);
-          }
+        const int ke = (t0 + lr < row_end) ? kout : 0;  // rows past the end: no entries read
+        for (int e = j; e < ke; e += 4) {
+          const int c = ocol[lr * kout + e] & (kHeadDim - 1);
+          const float x = __half2float(oval[lr * kout + e]);
+          float z0 = 0.0f;
+          if (C::KCH) z0 = __high2float(reinterpret_cast<const __half2*>(km)[c]);
+          else if (!C::KSYM) z0 = __high2float(reinterpret_cast<const __half2*>(km)[lr * kgpr + c / Gk]);
+          add = fmaf(qf[c], x - z0, add);
         }
         add += __shfl_xor_sync(0xffffffffu, add, 1);
         add += __shfl_xor_sync(0xffffffffu, add, 2);
-        sc[it] += add;
+        if (t0 + lr < row_end) sc[it] += add;
       }
     }
 
@@ -315,9 +328,13 @@ __global__ void __launch_bounds__(kThreads, 4)
       l_run *= alpha;
       cb *= alpha;
       zacc *= alpha;
+      const uint64_t AL = f2_pack(alpha, alpha);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) acc[k] *= alpha;
-      if (kout > 0) {
+      for (int k = 0; k < 32; k += 2) {
+        const uint64_t A = f2_mul(AL, f2_pack(acc[k], acc[k + 1]));
+        f2_unpack(A, acc[k], acc[k + 1]);
+      }
+      if (OUTL) {
         __syncwarp();
 #pragma unroll
         for (int k = 0; k < 4; ++k) myoc[lane + 32 * k] *= alpha;
@@ -360,25 +377,27 @@ __global__ void __launch_bounds__(kThreads, 4)
       if (!C::VSYM) zacc = fmaf(p[it], zt, zacc);
       float f[32];
       Unpack<VB>::run(w, f);
+      const uint64_t PB = f2_pack(pb, pb);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) acc[k] = fmaf(pb, f[k], acc[k]);
+      for (int k = 0; k < 32; k += 2) {
+        const uint64_t A = f2_fma(PB, f2_pack(f[k], f[k + 1]), f2_pack(acc[k], acc[k + 1]));
+        f2_unpack(A, acc[k], acc[k + 1]);
+      }
     }
 
     // ---- value outliers: o_c += p_t (x - dequant(code 0)) ----------------------
-    if (kout > 0) {
+    if (OUTL) {
+      const uint16_t* vcol = ocol + C::OUT_ONE;
+      const __half* vval = reinterpret_cast<const __half*>(ocol + 3 * (C::OUT_ONE / 2));
 #pragma unroll
       for (int it = 0; it < 4; ++it) {
-        const int row = it * 8 + r8;
-        const int t = t0 + row;
-        if (t < row_end) {
-          const int32_t* rp = L.v.rowptr + (int64_t)n * L.v.rowptr_sstride;
-          const int beg = rp[t], end = rp[t + 1];
-          for (int e = beg + j; e < end; e += 4) {
-            const int64_t ei = (int64_t)n * L.v.out_sstride + e;
-            const int c = L.v.col[ei];
-            const float x = __half2float(L.v.val[ei]);
+        const int lr = it * 8 + r8;
+        if (t0 + lr < row_end) {
+          for (int e = j; e < kout; e += 4) {
+            const int c = vcol[lr * kout + e] & (kHeadDim - 1);
+            const float x = __half2float(vval[lr * kout + e]);
             float z0 = 0.0f;
-            if (!C::VSYM) z0 = __high2float(reinterpret_cast<const __half2*>(vm)[row * vgpr + c / Gv]);
+            if (!C::VSYM) z0 = __high2float(reinterpret_cast<const __half2*>(vm)[lr * vgpr + c / Gv]);
             atomicAdd(&myoc[c], p[it] * (x - z0));
           }
         }
@@ -456,22 +475,22 @@ __global__ void __launch_bounds__(kThreads, 4)
   }
 }
 
-template <int KB, int KMODE, int VB, int VMODE>
+template <int KB, int KMODE, int VB, int VMODE, bool OUTL>
 cudaError_t launch_t(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
-  using C = Cfg<KB, KMODE, VB, VMODE>;
+  using C = Cfg<KB, KMODE, VB, VMODE, OUTL>;
   const size_t sm = C::smem_bytes();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mha_kernel<KB, KMODE, VB, VMODE>,
+    cudaError_t e = cudaFuncSetAttribute(decode_mha_kernel<KB, KMODE, VB, VMODE, OUTL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (a.occupancy_out)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        a.occupancy_out, decode_mha_kernel<KB, KMODE, VB, VMODE>, kThreads, sm);
+        a.occupancy_out, decode_mha_kernel<KB, KMODE, VB, VMODE, OUTL>, kThreads, sm);
   dim3 grid(a.splits, L.n_streams);
-  decode_mha_kernel<KB, KMODE, VB, VMODE><<<grid, kThreads, sm, st>>>(L, a);
+  decode_mha_kernel<KB, KMODE, VB, VMODE, OUTL><<<grid, kThreads, sm, st>>>(L, a);
   return cudaGetLastError();
 }
 
