@@ -208,6 +208,7 @@ def run_gpu(args, wl, rank, world, device):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    launches0 = kvq.kernel_launches()
     with ClockSampler(device.index) as clk:
         barrier(device)
         torch.cuda.synchronize(device)
@@ -217,6 +218,7 @@ def run_gpu(args, wl, rank, world, device):
         t1.record(stream)
         torch.cuda.synchronize(device)
         barrier(device)
+    launches = kvq.kernel_launches() - launches0
     clocks = clk.summary()
     assert cache.status() == 0
     total_ms = t0.elapsed_time(t1)
@@ -282,7 +284,7 @@ def run_gpu(args, wl, rank, world, device):
                      "algorithmic_bytes": dom[2]},
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": launches,
     }
     return line
 
@@ -294,15 +296,19 @@ def codec_name(bits, mode, group):
 
 
 def load_traffic(wl, kernel):
-    """dram bytes per launch from the committed ncu summary, when one exists
-    for this workload and kernel (else null)."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch (read + write) from the committed ncu summary
+    profiles/traffic.txt, lines "<workload> <kernel> <bytes>", when it holds
+    this workload and kernel; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.txt")
     try:
         with open(p) as f:
-            d = json.load(f)
-        return d.get(wl.name, {}).get(kernel)
-    except Exception:
-        return None
+            for ln in f:
+                parts = ln.split()
+                if len(parts) == 3 and parts[0] == wl.name and parts[1] == kernel:
+                    return int(float(parts[2]))
+    except OSError:
+        pass
+    return None
 
 
 def run_e2e(args, wl, cache, k, v, q, k1, v1, out, ws, scale, device, b_step):
@@ -384,15 +390,22 @@ def oracle_step_on_sample(wl, n_streams, seed):
 
 
 def cpu_sample(wl, budget_s):
-    """Times the oracle on as many streams as fit about budget_s seconds."""
+    """Times the oracle on a bounded sample of the workload: as many (batch,
+    kv-head) streams as one batch holds, repeated until about budget_s seconds
+    of CPU work have been spent."""
     dt1, _ = oracle_step_on_sample(wl, 1, wl.seed)
     n = max(1, min(wl.num_kv_heads, int(budget_s / max(dt1, 1e-3))))
-    dt, b = oracle_step_on_sample(wl, n, wl.seed) if n > 1 else oracle_step_on_sample(wl, 1, wl.seed)
-    return {"value": round(b / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d of %d (batch, kv-head) streams at the full context %d, one full "
-                      "step (prefill + append + decode), numpy single thread"
-                      % (n, wl.batch * wl.num_kv_heads, wl.seq_len),
-            "seconds": round(dt, 2)}
+    tot_s, tot_b, reps = 0.0, 0.0, 0
+    while reps == 0 or tot_s < 0.8 * budget_s:
+        dt, b = oracle_step_on_sample(wl, n, wl.seed + reps)
+        tot_s += dt
+        tot_b += b
+        reps += 1
+    return {"value": round(tot_b / tot_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": "%d x %d of %d (batch, kv-head) streams at the full context %d, one full "
+                      "step each (prefill + append + decode), numpy single thread"
+                      % (reps, n, wl.batch * wl.num_kv_heads, wl.seq_len),
+            "seconds": round(tot_s, 2)}
 
 
 def run_reference(args, wl, rank, world):
@@ -429,6 +442,33 @@ def run_reference(args, wl, rank, world):
     }
 
 
+def profile_case(args, wl):
+    """A short untimed run for profilers: prefill, append and decode of the
+    workload's codec and shape at a reduced batch, args.reps times."""
+    import dataclasses
+    import bit_quantized_kv_kvq_gb300 as kvq
+    from bit_quantized_kv_kvq_gb300.synth import LayerSource
+
+    if args.batch:
+        wl = dataclasses.replace(wl, batch=args.batch)
+    device = torch.device("cuda", 0)
+    S = wl.seq_len
+    cache = kvq.QuantizedKVCache(1, wl.batch, wl.num_kv_heads, wl.head_dim, S + 1, wl.k_bits,
+                                 wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group, wl.v_group,
+                                 wl.outliers_per_row, device=device)
+    src = LayerSource(wl, 0, device=device)
+    k, v = src.kv(S)
+    q, k1, v1 = src.step(0)
+    for _ in range(args.reps):
+        cache.prefill(0, k, v)
+        cache.append(0, k1, v1)
+        cache.decode(0, q, 1.0 / math.sqrt(wl.head_dim))
+    torch.cuda.synchronize(device)
+    if cache.status() != 0:
+        raise RuntimeError("device status word %#x" % cache.status())
+    print(json.dumps({"profile_case": wl.name, "batch": wl.batch, "reps": args.reps}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -438,10 +478,17 @@ def main(argv=None):
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", action="store_true",
+                    help="untimed prefill/append/decode repetitions for a profiler")
+    ap.add_argument("--batch", type=int, default=0, help="batch of --profile-case (0: workload's)")
+    ap.add_argument("--reps", type=int, default=2, help="repetitions of --profile-case")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     wl = W.BY_NAME[args.workload]
+    if args.profile_case:
+        profile_case(args, wl)
+        return 0
     rank, world, local = dist_env()
     if args.impl == "reference":
         line = run_reference(args, wl, rank, world)

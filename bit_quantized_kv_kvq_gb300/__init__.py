@@ -95,8 +95,15 @@ def lib():
         L.kvq_last_error.restype = ctypes.c_char_p
         L.kvq_version.argtypes = []
         L.kvq_version.restype = ctypes.c_int32
+        L.kvq_kernel_launches.argtypes = []
+        L.kvq_kernel_launches.restype = ctypes.c_uint64
         _lib = L
     return _lib
+
+
+def kernel_launches() -> int:
+    """Device kernels this process has enqueued through the library."""
+    return int(lib().kvq_kernel_launches())
 
 
 def check(status):

@@ -41,31 +41,30 @@ bool decode_supported(const LayerDev& L, int gqa) {
 
 cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
   cudaError_t e;
+  const int rows = (L.n_streams / L.num_kv_heads) * a.num_q_heads;
+  bool combine = true;
   if (a.gqa == 1 && decode_mha_supported(L)) {
     e = launch_decode_mha(L, a, st);
-    if (e != cudaSuccess || a.splits == 1 || a.occupancy_out) return e;  // one split writes the output itself
-    const int rows = (L.n_streams / L.num_kv_heads) * a.num_q_heads;
-    combine_kernel<<<rows, kHeadDim, 0, st>>>(a.part_o, a.part_ml, a.splits, a.out, a.out_dtype);
-    return cudaGetLastError();
-  }
-  if (a.gqa > 1 && decode_gqa_supported(L, a.gqa)) {
+    combine = a.splits > 1;  // one split writes the output itself
+  } else if (a.gqa > 1 && decode_gqa_supported(L, a.gqa)) {
     e = launch_decode_gqa(L, a, st);
-    if (e != cudaSuccess || a.splits == 1 || a.occupancy_out) return e;
-    const int rows = (L.n_streams / L.num_kv_heads) * a.num_q_heads;
-    combine_kernel<<<rows, kHeadDim, 0, st>>>(a.part_o, a.part_ml, a.splits, a.out, a.out_dtype);
-    return cudaGetLastError();
-  }
-  switch (a.gqa) {
-    case 1: e = launch_decode_g1(L, a, st); break;
-    case 2: e = launch_decode_g2(L, a, st); break;
-    case 4: e = launch_decode_g4(L, a, st); break;
-    case 8: e = launch_decode_g8(L, a, st); break;
-    default: return cudaErrorNotSupported;
+    combine = a.splits > 1;
+  } else {
+    switch (a.gqa) {
+      case 1: e = launch_decode_g1(L, a, st); break;
+      case 2: e = launch_decode_g2(L, a, st); break;
+      case 4: e = launch_decode_g4(L, a, st); break;
+      case 8: e = launch_decode_g8(L, a, st); break;
+      default: return cudaErrorNotSupported;
+    }
   }
   if (e != cudaSuccess || a.occupancy_out) return e;
-  const int rows = (a.out == nullptr) ? 0 : (L.n_streams / L.num_kv_heads) * a.num_q_heads;
+  count_launches(1);
+  if (!combine) return cudaSuccess;
   combine_kernel<<<rows, kHeadDim, 0, st>>>(a.part_o, a.part_ml, a.splits, a.out, a.out_dtype);
-  return cudaGetLastError();
+  e = cudaGetLastError();
+  if (e == cudaSuccess) count_launches(1);
+  return e;
 }
 
 }  // namespace kvq

@@ -5,6 +5,7 @@
 
 #include <cstdarg>
 #include <cstdio>
+#include <atomic>
 #include <cstring>
 #include <string>
 #include <vector>
@@ -254,6 +255,9 @@ kvq_status check_layer(const kvq_cache* h, int layer) {
 
 namespace kvq {
 void set_error_message(const char* msg) { g_err = msg ? msg : ""; }
+
+static std::atomic<uint64_t> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 }  // namespace kvq
 
 extern "C" {
@@ -321,6 +325,7 @@ kvq_status kvq_prefill_quantize(kvq_cache* h, int32_t layer, const void* k, cons
                                       static_cast<const __half*>(v), seq_len,
                                       static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+  if (seq_len > 0) kvq::count_launches(1);
   h->len[layer] = seq_len;
   return KVQ_OK;
 }
@@ -340,6 +345,7 @@ kvq_status kvq_append_quantize(kvq_cache* h, int32_t layer, const void* k, const
                                      static_cast<const __half*>(v), pos,
                                      static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "append launch");
+  kvq::count_launches(1);
   h->len[layer] = pos + 1;
   return KVQ_OK;
 }
@@ -476,6 +482,8 @@ kvq_status kvq_cache_status(kvq_cache* h, void* stream, uint32_t* word) {
 }
 
 const char* kvq_last_error(void) { return g_err.c_str(); }
+
+uint64_t kvq_kernel_launches(void) { return kvq::g_launches.load(std::memory_order_relaxed); }
 
 int32_t kvq_version(void) { return 100; }
 

@@ -79,6 +79,9 @@ cudaError_t launch_decode_mha(const LayerDev& L, const DecodeArgs& a, cudaStream
 bool decode_gqa_supported(const LayerDev& L, int gqa);
 cudaError_t launch_decode_gqa(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);
 
+// Adds n to the process-wide count returned by kvq_kernel_launches().
+void count_launches(int n);
+
 // Replaces the thread-local message returned by kvq_last_error().
 void set_error_message(const char* msg);
 

@@ -235,6 +235,12 @@ KVQ_API kvq_status kvq_cache_status(kvq_cache* cache, void* stream, uint32_t* wo
 /* Thread-local description of the last error ("" if none). */
 KVQ_API const char* kvq_last_error(void);
 
+/* Number of device kernels this process has enqueued through the library
+ * (all caches, all threads), counted on the host at each successful
+ * launch: prefill 1, append 1, decode 1 plus 1 for the split combine when
+ * the work was split. Occupancy queries launch nothing and are not counted. */
+KVQ_API uint64_t kvq_kernel_launches(void);
+
 /* Library version, major * 10000 + minor * 100 + patch. */
 KVQ_API int32_t kvq_version(void);
 

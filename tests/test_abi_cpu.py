@@ -37,6 +37,13 @@ def test_version(lib):
     assert lib.kvq_version() == 100
 
 
+def test_launch_counter_counts_nothing_without_work(lib):
+    before = kvq.kernel_launches()
+    with pytest.raises(kvq.KVQError):
+        kvq.check(lib.kvq_prefill_quantize(None, 0, None, None, 0, None))
+    assert kvq.kernel_launches() == before
+
+
 def _cfg(**kw):
     base = dict(num_layers=1, batch=2, num_kv_heads=4, head_dim=128, max_seq=1000, k_bits=4,
                 v_bits=4, k_mode=kvq.ASYM_PER_CHANNEL, v_mode=kvq.ASYM_PER_TOKEN, k_group=64,

@@ -168,3 +168,25 @@ def test_errors_are_reported_not_raised_on_device():
         cache.decode(0, q, 1.0, workspace=ws)
     assert e.value.status == 3
     assert cache.status() == 0
+
+
+def test_launch_counter_matches_the_work_enqueued():
+    """prefill, append and decode enqueue one kernel each, plus the split
+    combine when the decode was split."""
+    import bit_quantized_kv_kvq_gb300 as kvq
+    wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=4, num_kv_heads=4, seq_len=300)
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(wl.seq_len)
+    q, k1, v1 = src.step(0)
+    cache = K.make_gpu_cache(wl, 400)
+    n0 = kvq.kernel_launches()
+    cache.prefill(0, k.cuda(), v.cuda())
+    cache.append(0, k1.cuda(), v1.cuda())
+    assert kvq.kernel_launches() - n0 == 2
+    for splits, extra in ((1, 1), (3, 2)):
+        cache.set_decode_splits(splits)
+        n1 = kvq.kernel_launches()
+        cache.decode(0, q.cuda(), 0.1)
+        assert kvq.kernel_launches() - n1 == extra
+    torch.cuda.synchronize()
+    assert cache.status() == 0
