@@ -1,0 +1,34 @@
+// Dispatch of the prefill kernels without outliers and with 4- or 8-bit
+// codes (prefill_fast.cuh) for one value codec, chosen by the including
+// translation unit through KVQ_PF_VB and KVQ_PF_VSYM.
+#pragma once
+#include "prefill_fast.cuh"
+
+namespace kvq {
+
+#ifndef KVQ_PF_VB
+#error "KVQ_PF_VB (4 or 8) and KVQ_PF_VSYM (0 or 1) select the value codec of this unit"
+#endif
+
+#define KVQ_PF_NAME3(a, b, c) a##b##c
+#define KVQ_PF_NAME(b, c) KVQ_PF_NAME3(launch_prefill_fast_v, b, c)
+
+cudaError_t KVQ_PF_NAME(KVQ_PF_VB, KVQ_PF_VSYM)(const LayerDev& L, const __half* k,
+                                                 const __half* v, int seq_len, cudaStream_t st) {
+  constexpr int VB = KVQ_PF_VB;
+  constexpr bool VS = KVQ_PF_VSYM != 0;
+  const TensorDev& K = L.k;
+  if (K.mode == KVQ_ASYM_PER_CHANNEL) {
+    if (K.bits == 4) {
+      if (K.group == 64) return pfx::launch_fast_t<4, KVQ_ASYM_PER_CHANNEL, 64, VB, VS>(L, k, v, seq_len, st);
+      return pfx::launch_fast_t<4, KVQ_ASYM_PER_CHANNEL, 128, VB, VS>(L, k, v, seq_len, st);
+    }
+    if (K.group == 64) return pfx::launch_fast_t<8, KVQ_ASYM_PER_CHANNEL, 64, VB, VS>(L, k, v, seq_len, st);
+    return pfx::launch_fast_t<8, KVQ_ASYM_PER_CHANNEL, 128, VB, VS>(L, k, v, seq_len, st);
+  }
+  if (K.mode == KVQ_SYM_PER_TOKEN) return pfx::launch_fast_t<8, KVQ_SYM_PER_TOKEN, 1, VB, VS>(L, k, v, seq_len, st);
+  if (K.bits == 4) return pfx::launch_fast_t<4, KVQ_ASYM_PER_TOKEN, 1, VB, VS>(L, k, v, seq_len, st);
+  return pfx::launch_fast_t<8, KVQ_ASYM_PER_TOKEN, 1, VB, VS>(L, k, v, seq_len, st);
+}
+
+}  // namespace kvq

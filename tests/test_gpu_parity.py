@@ -190,3 +190,80 @@ def test_launch_counter_matches_the_work_enqueued():
         assert kvq.kernel_launches() - n1 == extra
     torch.cuda.synchronize()
     assert cache.status() == 0
+
+
+NO_OUTLIER_CODECS = [
+    ("k4c64_v4g64", dict(k_bits=4, v_bits=4, k_mode=W.ASYM_PER_CHANNEL, v_mode=W.ASYM_PER_TOKEN,
+                         k_group=64, v_group=64)),
+    ("k8c128_v8g32", dict(k_bits=8, v_bits=8, k_mode=W.ASYM_PER_CHANNEL, v_mode=W.ASYM_PER_TOKEN,
+                          k_group=128, v_group=32)),
+    ("k4c128_v8g128", dict(k_bits=4, v_bits=8, k_mode=W.ASYM_PER_CHANNEL, v_mode=W.ASYM_PER_TOKEN,
+                           k_group=128, v_group=128)),
+    ("k4t16_v4g16", dict(k_bits=4, v_bits=4, k_mode=W.ASYM_PER_TOKEN, v_mode=W.ASYM_PER_TOKEN,
+                         k_group=16, v_group=16)),
+    ("q8_g64", dict(k_bits=8, v_bits=8, k_mode=W.SYM_PER_TOKEN, v_mode=W.SYM_PER_TOKEN,
+                    k_group=64, v_group=64)),
+]
+
+
+@pytest.mark.parametrize("seq", [1, 63, 64, 65, 127, 128, 129, 300])
+@pytest.mark.parametrize("name,codec", NO_OUTLIER_CODECS, ids=[c[0] for c in NO_OUTLIER_CODECS])
+def test_lengths_without_outliers(seq, name, codec):
+    wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=2, num_kv_heads=2, seq_len=seq,
+                 outliers_per_row=0, **codec)
+    _run_case(wl, appends=2, check_every=1)
+
+
+def _tie_inputs(wl, seed):
+    """fp16 K/V whose groups make many quotients exact ties k + 1/2: every
+    group holds multiples of step/2 (one power-of-two step per group) with
+    its extremes at 0 and lev * step (symmetric: -lev * step and lev * step),
+    so the scale is step. Plus a constant stretch (zero scales) and a
+    tiny-range stretch (subnormal fp16 scales)."""
+    g = torch.Generator().manual_seed(seed)
+    B, H, S, D = wl.batch, wl.num_kv_heads, wl.seq_len, wl.head_dim
+    out = []
+    for which in range(2):
+        mode = wl.k_mode if which == 0 else wl.v_mode
+        bits = wl.k_bits if which == 0 else wl.v_bits
+        grp = wl.k_group if which == 0 else wl.v_group
+        sym = mode == W.SYM_PER_TOKEN
+        lev = 2 ** (bits - 1) - 1 if sym else 2 ** bits - 1
+        half = torch.randint(0, 2 * lev + 1, (B, H, S, D), generator=g).double() / 2
+        if sym:
+            half = half * torch.where(torch.rand((B, H, S, D), generator=g) < 0.5, -1.0, 1.0)
+        if mode == W.ASYM_PER_CHANNEL:
+            nb = -(-S // grp)
+            step = 2.0 ** torch.randint(-6, 3, (B, H, nb, 1, D), generator=g).double()
+            step = step.expand(B, H, nb, grp, D).reshape(B, H, nb * grp, D)[:, :, :S]
+            x = half * step
+            x[:, :, 0::grp] = 0.0
+            x[:, :, 1::grp] = lev * step[:, :, 1::grp]
+        else:
+            step = 2.0 ** torch.randint(-6, 3, (B, H, S, D // grp, 1), generator=g).double()
+            x = half.reshape(B, H, S, D // grp, grp) * step
+            x[..., 0] = -lev * step[..., 0] if sym else 0.0
+            x[..., 1] = lev * step[..., 0]
+            x = x.reshape(B, H, S, D)
+        x16 = x.to(torch.float16)
+        x16[:, :, : S // 4] = torch.where(torch.arange(D) % 2 == 0, x16[:, :, : S // 4], 1.25)
+        tiny = torch.randint(0, lev + 1, (B, H, 128, D), generator=g).double() * 2.0 ** -20
+        x16[:, :, 256:384] = tiny.to(torch.float16)
+        x16[:, 1:, 256:384] += torch.tensor(0.5, dtype=torch.float16)
+        out.append(x16)
+    return out
+
+
+@pytest.mark.parametrize("name,codec", NO_OUTLIER_CODECS, ids=[c[0] for c in NO_OUTLIER_CODECS])
+def test_exact_ties_and_tiny_scales(name, codec):
+    wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=2, num_kv_heads=2, seq_len=400,
+                 outliers_per_row=0, **codec)
+    k, v = _tie_inputs(wl, 7)
+    cache = K.make_gpu_cache(wl, 420)
+    cache.prefill(0, k.cuda(), v.cuda())
+    oc = O.OracleCache(K.spec_of(wl), 2)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    torch.cuda.synchronize()
+    for n in range(2):
+        K.assert_state_equal(K.gpu_state(cache, 0, n), K.oracle_state(oc, n), "n=%d" % n)
+    assert cache.status() == 0
