@@ -31,6 +31,34 @@ __global__ void __launch_bounds__(kHeadDim)
 
 }  // namespace
 
+cudaError_t launch_decode_tc_k33(const LayerDev& L, const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_tc_k44(const LayerDev& L, const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_tc_k48(const LayerDev& L, const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_tc_k84(const LayerDev& L, const DecodeArgs& a, cudaStream_t st);
+cudaError_t launch_decode_tc_k88(const LayerDev& L, const DecodeArgs& a, cudaStream_t st);
+
+// Per-channel keys and asymmetric per-token values with 3/3, 4/4, 4/8, 8/4
+// or 8/8 bits (value groups of 64 or 128 channels; 128 at 3 bits): the
+// tensor-core kernels of decode_tc.cuh, for every query-group size.
+static bool decode_tc_supported(const LayerDev& L, int gqa) {
+  if (gqa != 1 && gqa != 2 && gqa != 4 && gqa != 8) return false;
+  if (L.k.mode != KVQ_ASYM_PER_CHANNEL || L.v.mode != KVQ_ASYM_PER_TOKEN) return false;
+  const int kb = L.k.bits, vb = L.v.bits;
+  if ((kb == 3) != (vb == 3)) return false;
+  if (vb == 3) return L.v.group == 128;
+  return L.v.group == 64 || L.v.group == 128;
+}
+
+static cudaError_t launch_decode_tc(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
+  switch (L.k.bits * 10 + L.v.bits) {
+    case 33: return launch_decode_tc_k33(L, a, st);
+    case 44: return launch_decode_tc_k44(L, a, st);
+    case 48: return launch_decode_tc_k48(L, a, st);
+    case 84: return launch_decode_tc_k84(L, a, st);
+    default: return launch_decode_tc_k88(L, a, st);
+  }
+}
+
 bool decode_supported(const LayerDev& L, int gqa) {
   if (gqa != 1 && gqa != 2 && gqa != 4 && gqa != 8) return false;
   const int km = L.k.mode, vm = L.v.mode;
@@ -43,7 +71,10 @@ cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t s
   cudaError_t e;
   const int rows = (L.n_streams / L.num_kv_heads) * a.num_q_heads;
   bool combine = true;
-  if (a.gqa == 1 && decode_mha_supported(L)) {
+  if (decode_tc_supported(L, a.gqa)) {
+    e = launch_decode_tc(L, a, st);
+    combine = a.splits > 1;  // one split writes the output itself
+  } else if (a.gqa == 1 && decode_mha_supported(L)) {
     e = launch_decode_mha(L, a, st);
     combine = a.splits > 1;  // one split writes the output itself
   } else if (a.gqa > 1 && decode_gqa_supported(L, a.gqa)) {

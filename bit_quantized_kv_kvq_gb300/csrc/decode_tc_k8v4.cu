@@ -1,0 +1,4 @@
+// Tensor-core decode kernels: 8-bit keys, 4-bit values.
+#define KVQ_TC_KB 8
+#define KVQ_TC_VB 4
+#include "decode_tc_dispatch.cuh"

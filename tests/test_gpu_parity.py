@@ -267,3 +267,50 @@ def test_exact_ties_and_tiny_scales(name, codec):
     for n in range(2):
         K.assert_state_equal(K.gpu_state(cache, 0, n), K.oracle_state(oc, n), "n=%d" % n)
     assert cache.status() == 0
+
+
+TC_CODECS = [
+    ("k3v3g128", dict(k_bits=3, v_bits=3, k_group=128, v_group=128)),
+    ("k4v4g64", dict(k_bits=4, v_bits=4, k_group=64, v_group=64)),
+    ("k4v4g128", dict(k_bits=4, v_bits=4, k_group=128, v_group=128)),
+    ("k4v8g64", dict(k_bits=4, v_bits=8, k_group=64, v_group=64)),
+    ("k8v4g64", dict(k_bits=8, v_bits=4, k_group=256, v_group=64)),
+    ("k8v8g128", dict(k_bits=8, v_bits=8, k_group=64, v_group=128)),
+]
+
+
+@pytest.mark.parametrize("outliers", [0, 2])
+@pytest.mark.parametrize("gqa", [1, 2, 4, 8])
+@pytest.mark.parametrize("name,codec", TC_CODECS, ids=[c[0] for c in TC_CODECS])
+def test_tensor_core_decode_grid(name, codec, gqa, outliers):
+    """Per-channel keys with per-token values at every query-group size, with
+    and without outliers, lengths with a ragged last tile and a key residual."""
+    wl = replace(W.LLAMA7B_16K, batch=1, num_kv_heads=2, num_q_heads=2 * gqa, seq_len=333,
+                 k_mode=W.ASYM_PER_CHANNEL, v_mode=W.ASYM_PER_TOKEN,
+                 outliers_per_row=outliers, **codec)
+    _run_case(wl, appends=2, check_every=1)
+
+
+def test_tensor_core_decode_wide_value_scales():
+    """Value groups whose scales span many powers of two (the fp16 operand
+    keeps its precision through the running exponent)."""
+    wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=8, num_kv_heads=2, seq_len=700,
+                 k_bits=4, v_bits=4, k_group=64, v_group=64, outliers_per_row=0)
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(wl.seq_len)
+    g = torch.Generator().manual_seed(3)
+    span = 2.0 ** torch.randint(-12, 9, (1, 2, wl.seq_len, 1), generator=g).double()
+    v = (v.double() * span).clamp(-60000, 60000).to(torch.float16)
+    k = (k.double() * 2.0 ** torch.randint(-6, 6, (1, 2, 1, 128), generator=g).double()).to(torch.float16)
+    q, _, _ = src.step(0)
+    cache = K.make_gpu_cache(wl, wl.seq_len)
+    cache.prefill(0, k.cuda(), v.cuda())
+    oc = O.OracleCache(K.spec_of(wl), 2)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    torch.cuda.synchronize()
+    for n in range(2):
+        K.assert_state_equal(K.gpu_state(cache, 0, n), K.oracle_state(oc, n))
+    for splits in (1, 3):
+        cache.set_decode_splits(splits)
+        o = cache.decode(0, q.cuda(), 0.088).cpu().double().reshape(2, 4, 128).numpy()
+        K.assert_attention_close(o, oc.decode(K.q_streams(q, wl), 0.088))
