@@ -321,485 +321,530 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
     key_slot<KB>(lane & 3, lane >> 2, k, cs[k], sh);
   }
 
+  // Per tile: front (wait for the copies, key operand rebuild, scores,
+  // outliers, tile max), middle (running max, probabilities, value outliers,
+  // value-scale exponents, P' per token with one head), back (PV, then the
+  // stage is refilled). Issuing QK^T of tile i+1 before PV of tile i was
+  // measured slower (register pressure), so the phases run in order.
   bool failed = false;
-  int ti = 0;
-  for (; ti < w_count; ++ti) {
-    const int s = ti % S;
-    const uint32_t par = (uint32_t)(ti / S) & 1u;
-    const int t0 = row_begin + (w_first + ti) * kRows;
-    const bool rt = t0 >= kq;
-    unsigned char* base = stage_ptr(s);
-    const uint32_t* kc_s = reinterpret_cast<const uint32_t*>(base);
-    const uint32_t* vc_s = reinterpret_cast<const uint32_t*>(base + C::KC);
-    const __half2* km = reinterpret_cast<const __half2*>(base + C::KC + C::VC);
-    const __half2* vm = reinterpret_cast<const __half2*>(base + C::KC + C::VC + C::KMETA);
-    const unsigned char* ot = base + C::KC + C::VC + C::KMETA + C::VMETA;
-    if (!mbar_wait_bounded(&wb[s], par)) {
-      failed = true;
-      break;
-    }
-    __syncwarp();
+  int fail_tile = 0;
+  float sc[NT][2][2], mx_n[NT], p[NT][2][2];
+  float vsf[VGPR];  // 2^(6 - ev[q])
+  uint32_t pw[VGPR];
+  const bool one_head = NT == 1 && G == 1;  // warp-uniform
 
-    // ---- key block change: rebuild the Q'' fragments and the bias -------------
-    if (!rt && (t0 / Gk) != cur_blk) {
-      cur_blk = t0 / Gk;
-      const int kt4 = lane & 3, kkc = lane >> 2;
-      float sv[4], zv[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 sz = __half22float2(km[cs[k]]);
-        sv[k] = sz.x;
-        zv[k] = sz.y;
-      }
-      float zp[H];
-#pragma unroll
-      for (int h = 0; h < H; ++h) {
-        zp[h] = 0.0f;
-        if (h < G) {
-          float v[4], mx = 0.0f;
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            v[k] = qm[h * kHeadDim + cs[k]] * sv[k];
-            mx = fmaxf(mx, fabsf(v[k]));
-            zp[h] = fmaf(qf[h * kHeadDim + cs[k]], zv[k], zp[h]);
-          }
-          // scale the head's operand so that its largest |Q''| lies in [2^14, 2^15)
-          const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(mx));
-          const int e = mb ? (int)(mb >> 23) - 127 : 0;
-          const float up = exp2i(14 - e);
-          const int lh = 8 * (h & 3) + kt4;  // lane of column 2(h&3) (hi); lh + 4 holds lo
-#pragma unroll
-          for (int j = 0; j < 2; ++j) {
-            uint32_t lo;
-            const uint32_t hi = split_pair(v[2 * j] * up, v[2 * j + 1] * up, lo);
-            frag[((lh * NT + (h >> 2)) * 8 + kkc) * 2 + j] = hi;
-            frag[(((lh + 4) * NT + (h >> 2)) * 8 + kkc) * 2 + j] = lo;
-          }
-          if (lane == 0) kbias[8 + h] = exp2i(24 - (14 - e));  // undoes 2^-24 and the head scale
-        }
-      }
-      // bias sum_c q_c z_c of every head: butterfly reduce-scatter (lane keeps
-      // head (lane >> 2) & (H - 1)), then the sum over the remaining lanes
-      {
-        float kept[H];
-#pragma unroll
-        for (int h = 0; h < H; ++h) kept[h] = zp[h];
-#pragma unroll
-        for (int half = H / 2, off = 8 * (H / 4); half >= 1; half >>= 1, off >>= 1) {
-          const bool upper = (lane & off) != 0;
-#pragma unroll
-          for (int i = 0; i < half; ++i) {
-            const float send = upper ? kept[i] : kept[i + half];
-            const float keep = upper ? kept[i + half] : kept[i];
-            kept[i] = keep + __shfl_xor_sync(kFull, send, off);
-          }
-        }
-        float tot = kept[0];
-        if (H == 4) tot += __shfl_xor_sync(kFull, tot, 16);
-        tot += __shfl_xor_sync(kFull, tot, 2);
-        tot += __shfl_xor_sync(kFull, tot, 1);
-        if ((lane & 3) == 0 && (lane >> 2) < H) kbias[(lane >> 2) & (H - 1)] = tot;
-      }
+  auto front = [&](int tj) -> bool {
+    {
+      if (!mbar_wait_bounded(&wb[tj % S], (uint32_t)(tj / S) & 1u)) return false;
       __syncwarp();
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-        for (int kc = 0; kc < 8; kc += 2) {
-          const uint4 v = *reinterpret_cast<const uint4*>(&frag[((lane * NT + nt) * 8 + kc) * 2]);
-          bq[nt][kc][0] = v.x;
-          bq[nt][kc][1] = v.y;
-          bq[nt][kc + 1][0] = v.z;
-          bq[nt][kc + 1][1] = v.w;
+      const int t0 = row_begin + (w_first + tj) * kRows;
+      const bool rt = t0 >= kq;
+      unsigned char* base = stage_ptr(tj % S);
+      const uint32_t* kc_s = reinterpret_cast<const uint32_t*>(base);
+      const uint32_t* vc_s = reinterpret_cast<const uint32_t*>(base + C::KC);
+      const __half2* km = reinterpret_cast<const __half2*>(base + C::KC + C::VC);
+      const __half2* vm = reinterpret_cast<const __half2*>(base + C::KC + C::VC + C::KMETA);
+      const unsigned char* ot = base + C::KC + C::VC + C::KMETA + C::VMETA;
+      (void)rt; (void)kc_s; (void)vc_s; (void)km; (void)vm; (void)ot;
+      // ---- key block change: rebuild the Q'' fragments and the bias -------------
+      if (!rt && (t0 / Gk) != cur_blk) {
+        cur_blk = t0 / Gk;
+        const int kt4 = lane & 3, kkc = lane >> 2;
+        float sv[4], zv[4];
+  #pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 sz = __half22float2(km[cs[k]]);
+          sv[k] = sz.x;
+          zv[k] = sz.y;
         }
-        kb[nt] = (4 * nt + t4 < G) ? kbias[4 * nt + t4] : 0.0f;
-        kf[nt] = (4 * nt + t4 < G) ? kbias[8 + 4 * nt + t4] : 0.0f;
-      }
-      __syncwarp();
-    }
-
-    // ---- scores: sc[nt][mt][r], rows 16 mt + g + 8 r, head 4 nt + t4 -----------
-    float sc[NT][2][2];
-    if (!rt) {
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const int r0 = 16 * mt + g, r1 = r0 + 8;
-        // one accumulator chain per head tile, two (even / odd chunks) when
-        // there is a single head tile
-        constexpr int CH = NT == 1 ? 2 : 1;
-        float acc[NT][CH][4];
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4 * CH; ++e) acc[nt][e >> 2][e & 3] = 0.0f;
-        if (KB == 4) {
-          const uint4 A0 = reinterpret_cast<const uint4*>(kc_s + r0 * 16)[t4];
-          const uint4 A1 = reinterpret_cast<const uint4*>(kc_s + r1 * 16)[t4];
-          const uint32_t w0[4] = {A0.x, A0.y, A0.z, A0.w}, w1[4] = {A1.x, A1.y, A1.z, A1.w};
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t x0 = w0[j] >> (8 * h), x1 = w1[j] >> (8 * h);
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma(acc[nt][h % CH], x0 & 0x000F000Fu, x1 & 0x000F000Fu, x0 & 0x00F000F0u, x1 & 0x00F000F0u,
-                    bq[nt][2 * j + h][0], bq[nt][2 * j + h][1]);
+        float zp[H];
+  #pragma unroll
+        for (int h = 0; h < H; ++h) {
+          zp[h] = 0.0f;
+          if (h < G) {
+            float v[4], mx = 0.0f;
+  #pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              v[k] = qm[h * kHeadDim + cs[k]] * sv[k];
+              mx = fmaxf(mx, fabsf(v[k]));
+              zp[h] = fmaf(qf[h * kHeadDim + cs[k]], zv[k], zp[h]);
             }
-          }
-        } else if (KB == 8) {
-#pragma unroll
-          for (int hq = 0; hq < 2; ++hq) {
-            const uint4 A0 = reinterpret_cast<const uint4*>(kc_s + r0 * 32)[2 * t4 + hq];
-            const uint4 A1 = reinterpret_cast<const uint4*>(kc_s + r1 * 32)[2 * t4 + hq];
-            const uint32_t w0[4] = {A0.x, A0.y, A0.z, A0.w}, w1[4] = {A1.x, A1.y, A1.z, A1.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const int kc = 4 * hq + j;
-#pragma unroll
-              for (int nt = 0; nt < NT; ++nt)
-                mma(acc[nt][j % CH], w0[j] & 0x00FF00FFu, w1[j] & 0x00FF00FFu, (w0[j] >> 8) & 0x00FF00FFu,
-                    (w1[j] >> 8) & 0x00FF00FFu, bq[nt][kc][0], bq[nt][kc][1]);
+            // scale the head's operand so that its largest |Q''| lies in [2^14, 2^15)
+            const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(mx));
+            const int e = mb ? (int)(mb >> 23) - 127 : 0;
+            const float up = exp2i(14 - e);
+            const int lh = 8 * (h & 3) + kt4;  // lane of column 2(h&3) (hi); lh + 4 holds lo
+  #pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              uint32_t lo;
+              const uint32_t hi = split_pair(v[2 * j] * up, v[2 * j + 1] * up, lo);
+              frag[((lh * NT + (h >> 2)) * 8 + kkc) * 2 + j] = hi;
+              frag[(((lh + 4) * NT + (h >> 2)) * 8 + kkc) * 2 + j] = lo;
             }
+            if (lane == 0) kbias[8 + h] = exp2i(24 - (14 - e));  // undoes 2^-24 and the head scale
           }
-        } else {
-          uint32_t P0[16], P1[16];
-#pragma unroll
-          for (int rr = 0; rr < 2; ++rr) {
-            const uint32_t* rw = kc_s + (rr ? r1 : r0) * 13;
-            uint32_t* P = rr ? P1 : P0;
-            const uint32_t X[3] = {rw[t4], rw[t4 + 4], rw[t4 + 8]};
-#pragma unroll
-            for (int i = 0; i < 3; ++i) {
-              P[4 * i + 0] = X[i] & 0x001C0007u;
-              P[4 * i + 1] = X[i] & 0x00E00038u;
-              P[4 * i + 2] = (X[i] >> 6) & 0x001C0007u;
-              P[4 * i + 3] = (X[i] >> 9) & 0x001C0007u;
-            }
-            const uint32_t ab = __byte_perm(X[0] >> 12, X[1] >> 12, 0x5410u);
-            const uint32_t cd = __byte_perm(X[2] >> 12, rw[12] >> (6 * t4), 0x5410u);
-            P[12] = ab & 0x00070007u;
-            P[13] = ab & 0x00380038u;
-            P[14] = cd & 0x00070007u;
-            P[15] = cd & 0x00380038u;
-          }
-#pragma unroll
-          for (int kc = 0; kc < 8; ++kc)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-              mma(acc[nt][kc % CH], P0[2 * kc], P1[2 * kc], P0[2 * kc + 1], P1[2 * kc + 1], bq[nt][kc][0],
-                  bq[nt][kc][1]);
         }
-#pragma unroll
+        // bias sum_c q_c z_c of every head: butterfly reduce-scatter (lane keeps
+        // head (lane >> 2) & (H - 1)), then the sum over the remaining lanes
+        {
+          float kept[H];
+  #pragma unroll
+          for (int h = 0; h < H; ++h) kept[h] = zp[h];
+  #pragma unroll
+          for (int half = H / 2, off = 8 * (H / 4); half >= 1; half >>= 1, off >>= 1) {
+            const bool upper = (lane & off) != 0;
+  #pragma unroll
+            for (int i = 0; i < half; ++i) {
+              const float send = upper ? kept[i] : kept[i + half];
+              const float keep = upper ? kept[i + half] : kept[i];
+              kept[i] = keep + __shfl_xor_sync(kFull, send, off);
+            }
+          }
+          float tot = kept[0];
+          if (H == 4) tot += __shfl_xor_sync(kFull, tot, 16);
+          tot += __shfl_xor_sync(kFull, tot, 2);
+          tot += __shfl_xor_sync(kFull, tot, 1);
+          if ((lane & 3) == 0 && (lane >> 2) < H) kbias[(lane >> 2) & (H - 1)] = tot;
+        }
+        __syncwarp();
+  #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          float c0 = acc[nt][0][0] + acc[nt][0][1], c1 = acc[nt][0][2] + acc[nt][0][3];
-          if (CH == 2) {
-            c0 += acc[nt][CH - 1][0] + acc[nt][CH - 1][1];
-            c1 += acc[nt][CH - 1][2] + acc[nt][CH - 1][3];
+  #pragma unroll
+          for (int kc = 0; kc < 8; kc += 2) {
+            const uint4 v = *reinterpret_cast<const uint4*>(&frag[((lane * NT + nt) * 8 + kc) * 2]);
+            bq[nt][kc][0] = v.x;
+            bq[nt][kc][1] = v.y;
+            bq[nt][kc + 1][0] = v.z;
+            bq[nt][kc + 1][1] = v.w;
           }
-          sc[nt][mt][0] = fmaf(c0, kf[nt], kb[nt]);
-          sc[nt][mt][1] = fmaf(c1, kf[nt], kb[nt]);
+          kb[nt] = (4 * nt + t4 < G) ? kbias[4 * nt + t4] : 0.0f;
+          kf[nt] = (4 * nt + t4 < G) ? kbias[8 + 4 * nt + t4] : 0.0f;
         }
+        __syncwarp();
       }
-    } else {
-      // fp16 residual keys (the last partial key block) on the CUDA cores
-      const __half* res = L.k.resid + (int64_t)n * L.k.resid_sstride + (int64_t)(t0 - kq) * kHeadDim;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int r = 0; r < 2; ++r) {
-            const int row = 16 * mt + g + 8 * r, h = 4 * nt + t4;
-            float d = 0.0f;
-            if (t0 + row < row_end && h < G) {
-              const __half2* kr = reinterpret_cast<const __half2*>(res + (size_t)row * kHeadDim);
-              const float* qh = qf + h * kHeadDim;
-              for (int c2 = 0; c2 < kHeadDim / 2; ++c2) {
-                const float2 x = __half22float2(kr[c2]);
-                d = fmaf(qh[2 * c2], x.x, fmaf(qh[2 * c2 + 1], x.y, d));
+
+      // ---- scores: sc[nt][mt][r], rows 16 mt + g + 8 r, head 4 nt + t4 -----------
+      if (!rt) {
+  #pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int r0 = 16 * mt + g, r1 = r0 + 8;
+          // one accumulator chain per head tile, two (even / odd chunks) when
+          // there is a single head tile
+          constexpr int CH = NT == 1 ? 2 : 1;
+          float acc[NT][CH][4];
+  #pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+            for (int e = 0; e < 4 * CH; ++e) acc[nt][e >> 2][e & 3] = 0.0f;
+          if (KB == 4) {
+            const uint4 A0 = reinterpret_cast<const uint4*>(kc_s + r0 * 16)[t4];
+            const uint4 A1 = reinterpret_cast<const uint4*>(kc_s + r1 * 16)[t4];
+            const uint32_t w0[4] = {A0.x, A0.y, A0.z, A0.w}, w1[4] = {A1.x, A1.y, A1.z, A1.w};
+  #pragma unroll
+            for (int j = 0; j < 4; ++j) {
+  #pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                const uint32_t x0 = w0[j] >> (8 * h), x1 = w1[j] >> (8 * h);
+  #pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                  mma(acc[nt][h % CH], x0 & 0x000F000Fu, x1 & 0x000F000Fu, x0 & 0x00F000F0u, x1 & 0x00F000F0u,
+                      bq[nt][2 * j + h][0], bq[nt][2 * j + h][1]);
               }
             }
-            sc[nt][mt][r] = d;
+          } else if (KB == 8) {
+  #pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+              const uint4 A0 = reinterpret_cast<const uint4*>(kc_s + r0 * 32)[2 * t4 + hq];
+              const uint4 A1 = reinterpret_cast<const uint4*>(kc_s + r1 * 32)[2 * t4 + hq];
+              const uint32_t w0[4] = {A0.x, A0.y, A0.z, A0.w}, w1[4] = {A1.x, A1.y, A1.z, A1.w};
+  #pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int kc = 4 * hq + j;
+  #pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                  mma(acc[nt][j % CH], w0[j] & 0x00FF00FFu, w1[j] & 0x00FF00FFu, (w0[j] >> 8) & 0x00FF00FFu,
+                      (w1[j] >> 8) & 0x00FF00FFu, bq[nt][kc][0], bq[nt][kc][1]);
+              }
+            }
+          } else {
+            uint32_t P0[16], P1[16];
+  #pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+              const uint32_t* rw = kc_s + (rr ? r1 : r0) * 13;
+              uint32_t* P = rr ? P1 : P0;
+              const uint32_t X[3] = {rw[t4], rw[t4 + 4], rw[t4 + 8]};
+  #pragma unroll
+              for (int i = 0; i < 3; ++i) {
+                P[4 * i + 0] = X[i] & 0x001C0007u;
+                P[4 * i + 1] = X[i] & 0x00E00038u;
+                P[4 * i + 2] = (X[i] >> 6) & 0x001C0007u;
+                P[4 * i + 3] = (X[i] >> 9) & 0x001C0007u;
+              }
+              const uint32_t ab = __byte_perm(X[0] >> 12, X[1] >> 12, 0x5410u);
+              const uint32_t cd = __byte_perm(X[2] >> 12, rw[12] >> (6 * t4), 0x5410u);
+              P[12] = ab & 0x00070007u;
+              P[13] = ab & 0x00380038u;
+              P[14] = cd & 0x00070007u;
+              P[15] = cd & 0x00380038u;
+            }
+  #pragma unroll
+            for (int kc = 0; kc < 8; ++kc)
+  #pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+                mma(acc[nt][kc % CH], P0[2 * kc], P1[2 * kc], P0[2 * kc + 1], P1[2 * kc + 1], bq[nt][kc][0],
+                    bq[nt][kc][1]);
           }
-    }
-
-    // ---- key outliers: score += q_c (x - z_c), one row per lane ---------------
-    if (OUTL) {
-      if (!rt) {
-        const __half* kval = reinterpret_cast<const __half*>(ot + 2 * kRows * kout);
-        const int ke = (t0 + lane < row_end) ? kout : 0;
-        const uint16_t* kcol = reinterpret_cast<const uint16_t*>(ot);
-        float corr[H];
-#pragma unroll
-        for (int h = 0; h < H; ++h) corr[h] = 0.0f;
-        for (int e = 0; e < ke; ++e) {
-          const int c = kcol[lane * kout + e] & (kHeadDim - 1);
-          const float d = __half2float(kval[lane * kout + e]) - __high2float(km[c]);
-#pragma unroll
-          for (int h = 0; h < H; ++h) corr[h] = fmaf(qf[h * kHeadDim + c], d, corr[h]);
-        }
-#pragma unroll
-        for (int h = 0; h < H; ++h) ocs[lane * H + h] = corr[h];
-        __syncwarp();
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int r = 0; r < 2; ++r) sc[nt][mt][r] += ocs[(16 * mt + g + 8 * r) * H + 4 * nt + t4];
-        __syncwarp();
-      }
-    }
-
-    // ---- online softmax (per thread: head 4 nt + t4) --------------------------
-    float p[NT][2][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const bool hv = 4 * nt + t4 < G;
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r)
-          if (!hv || t0 + 16 * mt + g + 8 * r >= row_end) sc[nt][mt][r] = -INFINITY;
-      float mt_ = fmaxf(fmaxf(sc[nt][0][0], sc[nt][0][1]), fmaxf(sc[nt][1][0], sc[nt][1][1]));
-      mt_ = fmaxf(mt_, __shfl_xor_sync(kFull, mt_, 4));
-      mt_ = fmaxf(mt_, __shfl_xor_sync(kFull, mt_, 8));
-      mt_ = fmaxf(mt_, __shfl_xor_sync(kFull, mt_, 16));
-      const bool up = mt_ > m_run[nt] + kLazy;
-      if (__any_sync(kFull, up)) {
-        const float mnew = up ? mt_ : m_run[nt];
-        const float al = up ? exp2f(m_run[nt] - mnew) : 1.0f;
-        l_run[nt] *= al;
-#pragma unroll
-        for (int q = 0; q < VGPR; ++q) zacc[nt][q] *= al;
-#pragma unroll
-        for (int mv = 0; mv < C::MTV; ++mv)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) o[mv][nt][e] *= al;
-        if (OUTL) {
-          // output corrections of head h follow that head's factor
-          __syncwarp();
-#pragma unroll
-          for (int hh = 0; hh < 4; ++hh) {
-            const float alh = __shfl_sync(kFull, al, hh);
-            const int h = 4 * nt + hh;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) ocr[h * kHeadDim + lane + 32 * k] *= alh;
-          }
-          __syncwarp();
-        }
-        m_run[nt] = mnew;
-      }
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          p[nt][mt][r] = sc[nt][mt][r] == -INFINITY ? 0.0f : exp2f(sc[nt][mt][r] - m_run[nt]);
-          l_run[nt] += p[nt][mt][r];
-        }
-    }
-
-    // ---- value outliers: o_c += p_t (x - z_t), one row per lane ----------------
-    if (OUTL) {
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int r = 0; r < 2; ++r) pst[(16 * mt + g + 8 * r) * H + 4 * nt + t4] = p[nt][mt][r];
-      __syncwarp();
-      if (t0 + lane < row_end) {
-        const uint16_t* vcol = reinterpret_cast<const uint16_t*>(ot + 4 * kRows * kout);
-        const __half* vval = reinterpret_cast<const __half*>(ot + 6 * kRows * kout);
-        for (int e = 0; e < kout; ++e) {
-          const int c = vcol[lane * kout + e] & (kHeadDim - 1);
-          const float d = __half2float(vval[lane * kout + e]) - __high2float(vm[lane * VGPR + c / VG]);
-          for (int h = 0; h < G; ++h) atomicAdd(&ocr[h * kHeadDim + c], pst[lane * H + h] * d);
-        }
-      }
-      __syncwarp();
-    }
-
-    // ---- value scale exponents of the tile (per group; lane = row), rescale
-    //      the group's accumulators when one grows -------------------------------
-    float vsf[VGPR];  // 2^(6 - ev[q])
-#pragma unroll
-    for (int q = 0; q < VGPR; ++q) {
-      const float sl = (t0 + lane < row_end) ? __low2float(vm[lane * VGPR + q]) : 0.0f;
-      const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(sl));
-      const int e = mb ? (int)(mb >> 23) - 127 : -127;
-      if (e > ev[q]) {  // warp-uniform
-        const float f = exp2i(max(ev[q] - e, -126));
-#pragma unroll
-        for (int mv = 0; mv < C::MTV; ++mv) {
-          int ch, sh, qq;
-          val_row<VB, VG>(mv, 0, 0, ch, sh, qq);
-          if (qq == q)
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-              for (int k = 0; k < 4; ++k) o[mv][nt][k] *= f;
-        }
-        ev[q] = e;
-      }
-      vsf[q] = exp2i(6 - ev[q]);
-    }
-
-    // ---- one query head: P' per token, one token per lane --------------------
-    // pw[q] = (lo, hi) fp16 pair of p_t s_t 2^(6 - ev[q]) for token t = lane
-    uint32_t pw[VGPR];
-    const bool one_head = NT == 1 && G == 1;  // warp-uniform
-    if (one_head) {
-      const int src = 4 * (lane & 7);  // head 0 lives in lanes with t4 = 0
-      const float p00 = __shfl_sync(kFull, p[0][0][0], src), p01 = __shfl_sync(kFull, p[0][0][1], src);
-      const float p10 = __shfl_sync(kFull, p[0][1][0], src), p11 = __shfl_sync(kFull, p[0][1][1], src);
-      const float pl = (lane & 16) ? ((lane & 8) ? p11 : p10) : ((lane & 8) ? p01 : p00);
-      const bool valid = t0 + lane < row_end;
-#pragma unroll
-      for (int q = 0; q < VGPR; ++q) {
-        const float2 sz = __half22float2(vm[lane * VGPR + q]);
-        zacc[0][q] = valid ? fmaf(pl, sz.y, zacc[0][q]) : zacc[0][q];
-        const float e = valid ? pl * (sz.x * vsf[q]) : 0.0f;
-        const float h = __half2float(__float2half_rn(e));
-        pw[q] = f2h2(__fsub_rn(e, h), e);
-      }
-    }
-
-    // ---- PV per 16-token step --------------------------------------------------
-#pragma unroll
-    for (int ks = 0; ks < 2; ++ks) {
-      // B operands P' = p s_t per value group (hi/lo columns)
-      uint32_t bp[VGPR][NT][2];
-      const int rA = 16 * ks + g, rB = rA + 8;  // rows this thread owns in the C layout
-      const bool vA = t0 + rA < row_end, vB = t0 + rB < row_end;
-      const int L1 = 4 * (2 * t4) + (g >> 1), L2 = 4 * (2 * t4 + 1) + (g >> 1);
-      if (one_head) {
-        const uint32_t sel = (g & 1) ? 0x5410u : 0x7632u;
-        const int tk = 16 * ks + 2 * t4;
-#pragma unroll
-        for (int q = 0; q < VGPR; ++q) {
-          const uint32_t X1 = __shfl_sync(kFull, pw[q], tk), X2 = __shfl_sync(kFull, pw[q], tk + 1);
-          const uint32_t X3 = __shfl_sync(kFull, pw[q], tk + 8), X4 = __shfl_sync(kFull, pw[q], tk + 9);
-          bp[q][0][0] = __byte_perm(X1, X2, sel);
-          bp[q][0][1] = __byte_perm(X3, X4, sel);
-        }
-      } else {
-#pragma unroll
-        for (int q = 0; q < VGPR; ++q) {
-          const float2 szA = __half22float2(vm[rA * VGPR + q]);
-          const float2 szB = __half22float2(vm[rB * VGPR + q]);
-          const float sA = vA ? szA.x * vsf[q] : 0.0f, sB = vB ? szB.x * vsf[q] : 0.0f;
-          const float zA = vA ? szA.y : 0.0f, zB = vB ? szB.y : 0.0f;
-#pragma unroll
+  #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            zacc[nt][q] = fmaf(p[nt][ks][0], zA, fmaf(p[nt][ks][1], zB, zacc[nt][q]));
-            uint32_t lo;
-            const uint32_t hi = split_pair(p[nt][ks][0] * sA, p[nt][ks][1] * sB, lo);
-            const uint32_t H1 = __shfl_sync(kFull, hi, L1), H2 = __shfl_sync(kFull, hi, L2);
-            const uint32_t O1 = __shfl_sync(kFull, lo, L1), O2 = __shfl_sync(kFull, lo, L2);
-            const uint32_t X1 = (g & 1) ? O1 : H1, X2 = (g & 1) ? O2 : H2;
-            bp[q][nt][0] = __byte_perm(X1, X2, 0x5410u);
-            bp[q][nt][1] = __byte_perm(X1, X2, 0x7632u);
+            float c0 = acc[nt][0][0] + acc[nt][0][1], c1 = acc[nt][0][2] + acc[nt][0][3];
+            if (CH == 2) {
+              c0 += acc[nt][CH - 1][0] + acc[nt][CH - 1][1];
+              c1 += acc[nt][CH - 1][2] + acc[nt][CH - 1][3];
+            }
+            sc[nt][mt][0] = fmaf(c0, kf[nt], kb[nt]);
+            sc[nt][mt][1] = fmaf(c1, kf[nt], kb[nt]);
           }
-        }
-      }
-      // A operands: value codes of rows ra, ra+1 (k-slots 2t4, 2t4+1) and
-      // ra+8, ra+9 (2t4+8, 2t4+9)
-      const int ra = 16 * ks + 2 * t4;
-      const int rows[4] = {ra, ra + 1, ra + 8, ra + 9};
-      if (VB == 4) {
-        uint32_t vw[4][2];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const unsigned char* rp = reinterpret_cast<const unsigned char*>(vc_s + rows[k] * 16);
-          if (VG == 128) {
-            const uint2 u = *reinterpret_cast<const uint2*>(rp + 8 * g);
-            vw[k][0] = u.x;
-            vw[k][1] = u.y;
-          } else {  // VG == 64
-            vw[k][0] = *reinterpret_cast<const uint32_t*>(rp + 4 * g);
-            vw[k][1] = *reinterpret_cast<const uint32_t*>(rp + 32 + 4 * g);
-          }
-        }
-#pragma unroll
-        for (int mv = 0; mv < 8; ++mv) {
-          const uint32_t i = mv & 3;
-          const uint32_t sel = i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12);
-          const uint32_t x01 = __byte_perm(vw[0][mv >> 2], vw[1][mv >> 2], sel);
-          const uint32_t x23 = __byte_perm(vw[2][mv >> 2], vw[3][mv >> 2], sel);
-          const int q = mv / (VG / 16);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma(o[mv][nt], x01 & 0x000F000Fu, x01 & 0x00F000F0u, x23 & 0x000F000Fu, x23 & 0x00F000F0u,
-                bp[q][nt][0], bp[q][nt][1]);
-        }
-      } else if (VB == 8) {
-        uint32_t vw[4][4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const unsigned char* rp = reinterpret_cast<const unsigned char*>(vc_s + rows[k] * 32);
-          if (VG == 128) {
-            const uint4 u = *reinterpret_cast<const uint4*>(rp + 16 * g);
-            vw[k][0] = u.x; vw[k][1] = u.y; vw[k][2] = u.z; vw[k][3] = u.w;
-          } else {  // VG == 64
-            const uint2 u0 = *reinterpret_cast<const uint2*>(rp + 8 * g);
-            const uint2 u1 = *reinterpret_cast<const uint2*>(rp + 64 + 8 * g);
-            vw[k][0] = u0.x; vw[k][1] = u0.y; vw[k][2] = u1.x; vw[k][3] = u1.y;
-          }
-        }
-#pragma unroll
-        for (int mv = 0; mv < 8; ++mv) {
-          const uint32_t i = mv & 1;
-          const uint32_t sel = (2 * i) | ((2 * i + 1) << 4) | ((4 + 2 * i) << 8) | ((5 + 2 * i) << 12);
-          const uint32_t x01 = __byte_perm(vw[0][mv >> 1], vw[1][mv >> 1], sel);
-          const uint32_t x23 = __byte_perm(vw[2][mv >> 1], vw[3][mv >> 1], sel);
-          const int q = mv / (VG / 16);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma(o[mv][nt], x01 & 0x00FF00FFu, (x01 >> 8) & 0x00FF00FFu, x23 & 0x00FF00FFu,
-                (x23 >> 8) & 0x00FF00FFu, bp[q][nt][0], bp[q][nt][1]);
         }
       } else {
-        uint32_t vw[4][2];
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          vw[k][0] = vc_s[rows[k] * 13 + g];
-          vw[k][1] = (g + 8 <= 12) ? vc_s[rows[k] * 13 + g + 8] : 0u;
-        }
-        constexpr uint32_t kSel[4] = {0x5410u, 0x6521u, 0x7632u, 0x7733u};
-        constexpr int kSelOf[10] = {0, 0, 0, 1, 1, 1, 2, 2, 3, 3};
-        constexpr uint32_t kMask[10] = {0x00070007u, 0x00380038u, 0x01C001C0u, 0x000E000Eu,
-                                        0x00700070u, 0x03800380u, 0x001C001Cu, 0x00E000E0u,
-                                        0x00070007u, 0x00380038u};
-        uint32_t x[4][2][2];  // selector, word (g / g+8), row pair
-#pragma unroll
-        for (int sI = 0; sI < 4; ++sI)
-#pragma unroll
-          for (int wi = 0; wi < 2; ++wi) {
-            x[sI][wi][0] = __byte_perm(vw[0][wi], vw[1][wi], kSel[sI]);
-            x[sI][wi][1] = __byte_perm(vw[2][wi], vw[3][wi], kSel[sI]);
+        // fp16 residual keys (the last partial key block) on the CUDA cores
+        const __half* res = L.k.resid + (int64_t)n * L.k.resid_sstride + (int64_t)(t0 - kq) * kHeadDim;
+  #pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+            for (int r = 0; r < 2; ++r) {
+              const int row = 16 * mt + g + 8 * r, h = 4 * nt + t4;
+              float d = 0.0f;
+              if (t0 + row < row_end && h < G) {
+                const __half2* kr = reinterpret_cast<const __half2*>(res + (size_t)row * kHeadDim);
+                const float* qh = qf + h * kHeadDim;
+                for (int c2 = 0; c2 < kHeadDim / 2; ++c2) {
+                  const float2 x = __half22float2(kr[c2]);
+                  d = fmaf(qh[2 * c2], x.x, fmaf(qh[2 * c2 + 1], x.y, d));
+                }
+              }
+              sc[nt][mt][r] = d;
+            }
+      }
+
+      // ---- key outliers: score += q_c (x - z_c), one row per lane ---------------
+      if (OUTL) {
+        if (!rt) {
+          const __half* kval = reinterpret_cast<const __half*>(ot + 2 * kRows * kout);
+          const int ke = (t0 + lane < row_end) ? kout : 0;
+          const uint16_t* kcol = reinterpret_cast<const uint16_t*>(ot);
+          float corr[H];
+  #pragma unroll
+          for (int h = 0; h < H; ++h) corr[h] = 0.0f;
+          for (int e = 0; e < ke; ++e) {
+            const int c = kcol[lane * kout + e] & (kHeadDim - 1);
+            const float d = __half2float(kval[lane * kout + e]) - __high2float(km[c]);
+  #pragma unroll
+            for (int h = 0; h < H; ++h) corr[h] = fmaf(qf[h * kHeadDim + c], d, corr[h]);
           }
-#pragma unroll
-        for (int mv = 0; mv < 10; ++mv) {
-          const int sI = kSelOf[mv];
-          const uint32_t m = kMask[mv];
-#pragma unroll
+  #pragma unroll
+          for (int h = 0; h < H; ++h) ocs[lane * H + h] = corr[h];
+          __syncwarp();
+  #pragma unroll
           for (int nt = 0; nt < NT; ++nt)
-            mma(o[mv][nt], x[sI][0][0] & m, x[sI][1][0] & m, x[sI][0][1] & m, x[sI][1][1] & m,
-                bp[0][nt][0], bp[0][nt][1]);
+  #pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+              for (int r = 0; r < 2; ++r) sc[nt][mt][r] += ocs[(16 * mt + g + 8 * r) * H + 4 * nt + t4];
+          __syncwarp();
         }
       }
-    }
 
-    __syncwarp();
-    if (lane == 0 && ti + S < w_count) {
-      fence_proxy_async_smem();
-      issue(ti + S, s);
+      // ---- online softmax (per thread: head 4 nt + t4) --------------------------
+  #pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const bool hv = 4 * nt + t4 < G;
+  #pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+          for (int r = 0; r < 2; ++r)
+            if (!hv || t0 + 16 * mt + g + 8 * r >= row_end) sc[nt][mt][r] = -INFINITY;
+        float& mt_ = mx_n[nt];
+        mt_ = fmaxf(fmaxf(sc[nt][0][0], sc[nt][0][1]), fmaxf(sc[nt][1][0], sc[nt][1][1]));
+        mt_ = fmaxf(mt_, __shfl_xor_sync(kFull, mt_, 4));
+        mt_ = fmaxf(mt_, __shfl_xor_sync(kFull, mt_, 8));
+        mt_ = fmaxf(mt_, __shfl_xor_sync(kFull, mt_, 16));
+      }
     }
+    return true;
+  };
+
+  auto middle = [&](int tj) {
+      const int t0 = row_begin + (w_first + tj) * kRows;
+      const bool rt = t0 >= kq;
+      unsigned char* base = stage_ptr(tj % S);
+      const uint32_t* kc_s = reinterpret_cast<const uint32_t*>(base);
+      const uint32_t* vc_s = reinterpret_cast<const uint32_t*>(base + C::KC);
+      const __half2* km = reinterpret_cast<const __half2*>(base + C::KC + C::VC);
+      const __half2* vm = reinterpret_cast<const __half2*>(base + C::KC + C::VC + C::KMETA);
+      const unsigned char* ot = base + C::KC + C::VC + C::KMETA + C::VMETA;
+      (void)rt; (void)kc_s; (void)vc_s; (void)km; (void)vm; (void)ot;
+      // ---- online softmax, second half: move the running max, probabilities ----
+  #pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        const float mt_ = mx_n[nt];
+        const bool up = mt_ > m_run[nt] + kLazy;
+        if (__any_sync(kFull, up)) {
+          const float mnew = up ? mt_ : m_run[nt];
+          const float al = up ? exp2f(m_run[nt] - mnew) : 1.0f;
+          l_run[nt] *= al;
+  #pragma unroll
+          for (int q = 0; q < VGPR; ++q) zacc[nt][q] *= al;
+  #pragma unroll
+          for (int mv = 0; mv < C::MTV; ++mv)
+  #pragma unroll
+            for (int e = 0; e < 4; ++e) o[mv][nt][e] *= al;
+          if (OUTL) {
+            // output corrections of head h follow that head's factor
+            __syncwarp();
+  #pragma unroll
+            for (int hh = 0; hh < 4; ++hh) {
+              const float alh = __shfl_sync(kFull, al, hh);
+              const int h = 4 * nt + hh;
+  #pragma unroll
+              for (int k = 0; k < 4; ++k) ocr[h * kHeadDim + lane + 32 * k] *= alh;
+            }
+            __syncwarp();
+          }
+          m_run[nt] = mnew;
+        }
+  #pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+          for (int r = 0; r < 2; ++r) {
+            p[nt][mt][r] = sc[nt][mt][r] == -INFINITY ? 0.0f : exp2f(sc[nt][mt][r] - m_run[nt]);
+            l_run[nt] += p[nt][mt][r];
+          }
+      }
+
+      // ---- value outliers: o_c += p_t (x - z_t), one row per lane ----------------
+      if (OUTL) {
+  #pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+            for (int r = 0; r < 2; ++r) pst[(16 * mt + g + 8 * r) * H + 4 * nt + t4] = p[nt][mt][r];
+        __syncwarp();
+        if (t0 + lane < row_end) {
+          const uint16_t* vcol = reinterpret_cast<const uint16_t*>(ot + 4 * kRows * kout);
+          const __half* vval = reinterpret_cast<const __half*>(ot + 6 * kRows * kout);
+          for (int e = 0; e < kout; ++e) {
+            const int c = vcol[lane * kout + e] & (kHeadDim - 1);
+            const float d = __half2float(vval[lane * kout + e]) - __high2float(vm[lane * VGPR + c / VG]);
+            for (int h = 0; h < G; ++h) atomicAdd(&ocr[h * kHeadDim + c], pst[lane * H + h] * d);
+          }
+        }
+        __syncwarp();
+      }
+
+      // ---- value scale exponents of the tile (per group; lane = row), rescale
+      //      the group's accumulators when one grows -------------------------------
+  #pragma unroll
+      for (int q = 0; q < VGPR; ++q) {
+        const float sl = (t0 + lane < row_end) ? __low2float(vm[lane * VGPR + q]) : 0.0f;
+        const uint32_t mb = __reduce_max_sync(kFull, __float_as_uint(sl));
+        const int e = mb ? (int)(mb >> 23) - 127 : -127;
+        if (e > ev[q]) {  // warp-uniform
+          const float f = exp2i(max(ev[q] - e, -126));
+  #pragma unroll
+          for (int mv = 0; mv < C::MTV; ++mv) {
+            int ch, sh, qq;
+            val_row<VB, VG>(mv, 0, 0, ch, sh, qq);
+            if (qq == q)
+  #pragma unroll
+              for (int nt = 0; nt < NT; ++nt)
+  #pragma unroll
+                for (int k = 0; k < 4; ++k) o[mv][nt][k] *= f;
+          }
+          ev[q] = e;
+        }
+        vsf[q] = exp2i(6 - ev[q]);
+      }
+
+      // ---- one query head: P' per token, one token per lane --------------------
+      // pw[q] = (lo, hi) fp16 pair of p_t s_t 2^(6 - ev[q]) for token t = lane
+      if (one_head) {
+        const int src = 4 * (lane & 7);  // head 0 lives in lanes with t4 = 0
+        const float p00 = __shfl_sync(kFull, p[0][0][0], src), p01 = __shfl_sync(kFull, p[0][0][1], src);
+        const float p10 = __shfl_sync(kFull, p[0][1][0], src), p11 = __shfl_sync(kFull, p[0][1][1], src);
+        const float pl = (lane & 16) ? ((lane & 8) ? p11 : p10) : ((lane & 8) ? p01 : p00);
+        const bool valid = t0 + lane < row_end;
+  #pragma unroll
+        for (int q = 0; q < VGPR; ++q) {
+          const float2 sz = __half22float2(vm[lane * VGPR + q]);
+          zacc[0][q] = valid ? fmaf(pl, sz.y, zacc[0][q]) : zacc[0][q];
+          const float e = valid ? pl * (sz.x * vsf[q]) : 0.0f;
+          const float h = __half2float(__float2half_rn(e));
+          pw[q] = f2h2(__fsub_rn(e, h), e);
+        }
+      }
+
+  };
+
+  auto back = [&](int tj) {
+      const int t0 = row_begin + (w_first + tj) * kRows;
+      const bool rt = t0 >= kq;
+      unsigned char* base = stage_ptr(tj % S);
+      const uint32_t* kc_s = reinterpret_cast<const uint32_t*>(base);
+      const uint32_t* vc_s = reinterpret_cast<const uint32_t*>(base + C::KC);
+      const __half2* km = reinterpret_cast<const __half2*>(base + C::KC + C::VC);
+      const __half2* vm = reinterpret_cast<const __half2*>(base + C::KC + C::VC + C::KMETA);
+      const unsigned char* ot = base + C::KC + C::VC + C::KMETA + C::VMETA;
+      (void)rt; (void)kc_s; (void)vc_s; (void)km; (void)vm; (void)ot;
+      // ---- PV per 16-token step --------------------------------------------------
+  #pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        // B operands P' = p s_t per value group (hi/lo columns)
+        uint32_t bp[VGPR][NT][2];
+        const int rA = 16 * ks + g, rB = rA + 8;  // rows this thread owns in the C layout
+        const bool vA = t0 + rA < row_end, vB = t0 + rB < row_end;
+        const int L1 = 4 * (2 * t4) + (g >> 1), L2 = 4 * (2 * t4 + 1) + (g >> 1);
+        if (one_head) {
+          const uint32_t sel = (g & 1) ? 0x5410u : 0x7632u;
+          const int tk = 16 * ks + 2 * t4;
+  #pragma unroll
+          for (int q = 0; q < VGPR; ++q) {
+            const uint32_t X1 = __shfl_sync(kFull, pw[q], tk), X2 = __shfl_sync(kFull, pw[q], tk + 1);
+            const uint32_t X3 = __shfl_sync(kFull, pw[q], tk + 8), X4 = __shfl_sync(kFull, pw[q], tk + 9);
+            bp[q][0][0] = __byte_perm(X1, X2, sel);
+            bp[q][0][1] = __byte_perm(X3, X4, sel);
+          }
+        } else {
+  #pragma unroll
+          for (int q = 0; q < VGPR; ++q) {
+            const float2 szA = __half22float2(vm[rA * VGPR + q]);
+            const float2 szB = __half22float2(vm[rB * VGPR + q]);
+            const float sA = vA ? szA.x * vsf[q] : 0.0f, sB = vB ? szB.x * vsf[q] : 0.0f;
+            const float zA = vA ? szA.y : 0.0f, zB = vB ? szB.y : 0.0f;
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              zacc[nt][q] = fmaf(p[nt][ks][0], zA, fmaf(p[nt][ks][1], zB, zacc[nt][q]));
+              uint32_t lo;
+              const uint32_t hi = split_pair(p[nt][ks][0] * sA, p[nt][ks][1] * sB, lo);
+              const uint32_t H1 = __shfl_sync(kFull, hi, L1), H2 = __shfl_sync(kFull, hi, L2);
+              const uint32_t O1 = __shfl_sync(kFull, lo, L1), O2 = __shfl_sync(kFull, lo, L2);
+              const uint32_t X1 = (g & 1) ? O1 : H1, X2 = (g & 1) ? O2 : H2;
+              bp[q][nt][0] = __byte_perm(X1, X2, 0x5410u);
+              bp[q][nt][1] = __byte_perm(X1, X2, 0x7632u);
+            }
+          }
+        }
+        // A operands: value codes of rows ra, ra+1 (k-slots 2t4, 2t4+1) and
+        // ra+8, ra+9 (2t4+8, 2t4+9)
+        const int ra = 16 * ks + 2 * t4;
+        const int rows[4] = {ra, ra + 1, ra + 8, ra + 9};
+        if (VB == 4) {
+          uint32_t vw[4][2];
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const unsigned char* rp = reinterpret_cast<const unsigned char*>(vc_s + rows[k] * 16);
+            if (VG == 128) {
+              const uint2 u = *reinterpret_cast<const uint2*>(rp + 8 * g);
+              vw[k][0] = u.x;
+              vw[k][1] = u.y;
+            } else {  // VG == 64
+              vw[k][0] = *reinterpret_cast<const uint32_t*>(rp + 4 * g);
+              vw[k][1] = *reinterpret_cast<const uint32_t*>(rp + 32 + 4 * g);
+            }
+          }
+  #pragma unroll
+          for (int mv = 0; mv < 8; ++mv) {
+            const uint32_t i = mv & 3;
+            const uint32_t sel = i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12);
+            const uint32_t x01 = __byte_perm(vw[0][mv >> 2], vw[1][mv >> 2], sel);
+            const uint32_t x23 = __byte_perm(vw[2][mv >> 2], vw[3][mv >> 2], sel);
+            const int q = mv / (VG / 16);
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma(o[mv][nt], x01 & 0x000F000Fu, x01 & 0x00F000F0u, x23 & 0x000F000Fu, x23 & 0x00F000F0u,
+                  bp[q][nt][0], bp[q][nt][1]);
+          }
+        } else if (VB == 8) {
+          uint32_t vw[4][4];
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const unsigned char* rp = reinterpret_cast<const unsigned char*>(vc_s + rows[k] * 32);
+            if (VG == 128) {
+              const uint4 u = *reinterpret_cast<const uint4*>(rp + 16 * g);
+              vw[k][0] = u.x; vw[k][1] = u.y; vw[k][2] = u.z; vw[k][3] = u.w;
+            } else {  // VG == 64
+              const uint2 u0 = *reinterpret_cast<const uint2*>(rp + 8 * g);
+              const uint2 u1 = *reinterpret_cast<const uint2*>(rp + 64 + 8 * g);
+              vw[k][0] = u0.x; vw[k][1] = u0.y; vw[k][2] = u1.x; vw[k][3] = u1.y;
+            }
+          }
+  #pragma unroll
+          for (int mv = 0; mv < 8; ++mv) {
+            const uint32_t i = mv & 1;
+            const uint32_t sel = (2 * i) | ((2 * i + 1) << 4) | ((4 + 2 * i) << 8) | ((5 + 2 * i) << 12);
+            const uint32_t x01 = __byte_perm(vw[0][mv >> 1], vw[1][mv >> 1], sel);
+            const uint32_t x23 = __byte_perm(vw[2][mv >> 1], vw[3][mv >> 1], sel);
+            const int q = mv / (VG / 16);
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma(o[mv][nt], x01 & 0x00FF00FFu, (x01 >> 8) & 0x00FF00FFu, x23 & 0x00FF00FFu,
+                  (x23 >> 8) & 0x00FF00FFu, bp[q][nt][0], bp[q][nt][1]);
+          }
+        } else {
+          uint32_t vw[4][2];
+  #pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            vw[k][0] = vc_s[rows[k] * 13 + g];
+            vw[k][1] = (g + 8 <= 12) ? vc_s[rows[k] * 13 + g + 8] : 0u;
+          }
+          constexpr uint32_t kSel[4] = {0x5410u, 0x6521u, 0x7632u, 0x7733u};
+          constexpr int kSelOf[10] = {0, 0, 0, 1, 1, 1, 2, 2, 3, 3};
+          constexpr uint32_t kMask[10] = {0x00070007u, 0x00380038u, 0x01C001C0u, 0x000E000Eu,
+                                          0x00700070u, 0x03800380u, 0x001C001Cu, 0x00E000E0u,
+                                          0x00070007u, 0x00380038u};
+          uint32_t x[4][2][2];  // selector, word (g / g+8), row pair
+  #pragma unroll
+          for (int sI = 0; sI < 4; ++sI)
+  #pragma unroll
+            for (int wi = 0; wi < 2; ++wi) {
+              x[sI][wi][0] = __byte_perm(vw[0][wi], vw[1][wi], kSel[sI]);
+              x[sI][wi][1] = __byte_perm(vw[2][wi], vw[3][wi], kSel[sI]);
+            }
+  #pragma unroll
+          for (int mv = 0; mv < 10; ++mv) {
+            const int sI = kSelOf[mv];
+            const uint32_t m = kMask[mv];
+  #pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma(o[mv][nt], x[sI][0][0] & m, x[sI][1][0] & m, x[sI][0][1] & m, x[sI][1][1] & m,
+                  bp[0][nt][0], bp[0][nt][1]);
+          }
+        }
+      }
+
+      __syncwarp();
+      if (lane == 0 && tj + S < w_count) {
+        fence_proxy_async_smem();
+        issue(tj + S, tj % S);
+      }
+  };
+
+  for (int ti = 0; ti < w_count; ++ti) {
+    if (!front(ti)) {
+      failed = true;
+      fail_tile = ti;
+      break;
+    }
+    middle(ti);
+    back(ti);
   }
   if (failed && lane == 0) {
     raise_status(L.status, kStatusTimeout);
-    for (int tj = ti; tj < w_count && tj < ti + S; ++tj)
+    // copies still in flight: tiles fail_tile .. fail_tile + S - 1
+    const int end = fail_tile + S;
+    for (int tj = fail_tile; tj < w_count && tj < end; ++tj)
       (void)mbar_wait_bounded(&wb[tj % S], (uint32_t)(tj / S) & 1u);
   }
 

@@ -1,10 +1,12 @@
-// Prefill dispatch: codecs without outliers and with 4- or 8-bit codes run
-// the barrier-light kernel of prefill_fast.cuh; the rest (3-bit codes,
-// outliers, 256-token key blocks) the kernel of prefill_impl.cuh.
+// Prefill dispatch: codecs without outliers run the barrier-light kernel of
+// prefill_fast.cuh; the rest (outliers, 256-token key blocks) the kernel of
+// prefill_impl.cuh.
 #include "prefill_impl.cuh"
 
 namespace kvq {
 
+cudaError_t launch_prefill_fast_v30(const LayerDev& L, const __half* k, const __half* v, int seq_len,
+                                    cudaStream_t st);
 cudaError_t launch_prefill_fast_v40(const LayerDev& L, const __half* k, const __half* v, int seq_len,
                                     cudaStream_t st);
 cudaError_t launch_prefill_fast_v80(const LayerDev& L, const __half* k, const __half* v, int seq_len,
@@ -14,7 +16,6 @@ cudaError_t launch_prefill_fast_v81(const LayerDev& L, const __half* k, const __
 
 static bool fast_prefill_supported(const LayerDev& L) {
   if (L.outliers != 0) return false;
-  if (L.k.bits == 3 || L.v.bits == 3) return false;
   if (L.k.mode == KVQ_ASYM_PER_CHANNEL && L.k.group != 64 && L.k.group != 128) return false;
   return true;
 }
@@ -23,6 +24,7 @@ cudaError_t launch_prefill(const LayerDev& L, const __half* k, const __half* v, 
                            cudaStream_t st) {
   if (seq_len <= 0) return cudaSuccess;
   if (fast_prefill_supported(L)) {
+    if (L.v.bits == 3) return launch_prefill_fast_v30(L, k, v, seq_len, st);
     if (L.v.bits == 4) return launch_prefill_fast_v40(L, k, v, seq_len, st);
     if (L.v.mode == KVQ_SYM_PER_TOKEN) return launch_prefill_fast_v81(L, k, v, seq_len, st);
     return launch_prefill_fast_v80(L, k, v, seq_len, st);

@@ -1,4 +1,4 @@
-// Prefill quantize for codecs with 4- or 8-bit codes and no outliers.
+// Prefill quantize for codecs without outliers (3-, 4- or 8-bit codes).
 //
 // One launch quantizes a whole prompt of one layer. CTAs of four warps are
 // persistent and take work items in a fixed order: a per-channel key block
@@ -117,7 +117,7 @@ __device__ __forceinline__ int rne_prod(float d, float r) {
 // when e < -s * ulp(m-) / 2 (ulp(m-) = the spacing below m, half of ulp(m)
 // only at m = 1/2), and equals m otherwise; a quotient of exactly m rounds
 // to the even one of k and k + 1.
-static __device__ __noinline__ int resolve_code(float d, float s, int k) {
+__device__ __forceinline__ int resolve_code(float d, float s, int k) {
   const float m = (float)k + 0.5f;
   const float e = __fmaf_rn(-m, s, d);
   const float h = __uint_as_float((__float_as_uint(m) & 0x7F800000u) - (24u << 23));  // ulp(m) / 2
@@ -215,10 +215,10 @@ __device__ __forceinline__ void settle_chunk(uint32_t (&wa)[BITS / 4], const uin
 
 // Codes of one chunk by the IEEE quotient with the clamp (a subnormal
 // nonzero scale somewhere in the warp's rows).
-template <int BITS, bool SYM, class XAt, class ZAt, class SAt>
+template <int BITS, bool SYM, int LEV, class XAt, class ZAt, class SAt>
 __device__ __forceinline__ void slow_chunk(uint32_t (&wa)[BITS / 4], XAt x_at, ZAt nz_at, SAt s_at) {
   constexpr int kPer = 32 / BITS;
-  constexpr int kLev = SYM ? (1 << (BITS - 1)) - 1 : (1 << BITS) - 1;
+  constexpr int kLev = LEV;
 #pragma unroll
   for (int j = 0; j < BITS / 4; ++j) {
     uint32_t w = 0;
@@ -237,6 +237,23 @@ __device__ __forceinline__ void slow_chunk(uint32_t (&wa)[BITS / 4], XAt x_at, Z
   }
 }
 
+// Word w (ten 3-bit codes, top two bits zero; word 12 holds eight) of a row
+// whose 128 codes sit one per byte in shared memory (16-byte aligned).
+__device__ __forceinline__ uint32_t pack3_word(const unsigned char* row, int w) {
+  const int b0 = 10 * w, base = b0 & ~3;
+  const uint32_t u0 = *reinterpret_cast<const uint32_t*>(row + base);
+  const uint32_t u1 = *reinterpret_cast<const uint32_t*>(row + base + 4);
+  const uint32_t u2 = w < 12 ? *reinterpret_cast<const uint32_t*>(row + base + 8) : 0u;
+  const bool odd = b0 != base;  // the word starts at byte 2 of an aligned group
+  const uint32_t x0 = odd ? __byte_perm(u0, u1, 0x5432u) : u0;
+  const uint32_t x1 = odd ? __byte_perm(u1, u2, 0x5432u) : u1;
+  const uint32_t x2 = odd ? (u2 >> 16) : u2;
+  auto comb4 = [](uint32_t x) {
+    return (x & 0x7u) | ((x >> 5) & 0x38u) | ((x >> 10) & 0x1C0u) | ((x >> 15) & 0xE00u);
+  };
+  return comb4(x0) | (comb4(x1) << 12) | ((x2 & 0x7u) << 24) | (((x2 >> 8) & 0x7u) << 27);
+}
+
 // ---------------------------------------------------------------------------
 // Per-token rows. A warp owns kRowsPerItem / 4 rows of the item; eight lanes
 // code one row (16 channels each: 16-byte chunks 2q and 2q + 1, read in an
@@ -244,9 +261,11 @@ __device__ __forceinline__ void slow_chunk(uint32_t (&wa)[BITS / 4], XAt x_at, Z
 // ---------------------------------------------------------------------------
 template <int BITS, bool SYM, int RPW>
 __device__ __forceinline__ void rows_warp(const unsigned char* tile, const TensorDev& T, int n,
-                                          int row0, int nrows, int warp, int lane) {
+                                          int row0, int nrows, int warp, int lane,
+                                          unsigned char* rowbuf) {
   constexpr int kLev = SYM ? (1 << (BITS - 1)) - 1 : (1 << BITS) - 1;
-  constexpr int kWords = 128 * BITS / 32;
+  constexpr int kWords = Pack<BITS>::kWords;
+  constexpr int PB = BITS == 3 ? 8 : BITS;  // field width while coding (3-bit codes go one per byte)
   const int q = lane & 7, rr = lane >> 3;
   const int sw = q >> 2;
   const int lpg = T.group >> 4;  // lanes per group (groups of 16 .. 128 channels)
@@ -306,7 +325,7 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
       else
         reinterpret_cast<__half2*>(mb)[at] = __halves2half2(s16, z16);
     }
-    uint32_t wa0[BITS / 4], wb0[BITS / 4], wa1[BITS / 4], wb1[BITS / 4];
+    uint32_t wa0[PB / 4], wb0[PB / 4], wa1[PB / 4], wb1[PB / 4];
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(rowp);
     const Bcast<float> NZ{nz}, RL{rlo};
     auto xat0 = [&](int i) { return xs[8 * c0 + i]; };
@@ -315,20 +334,32 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
     auto sat = [&](int) { return s; };
     auto rat = [&](int) { return rlo; };
     if (!__any_sync(kFull, slow)) {
-      chunk_codes<BITS, SYM>(raw0, NZ, RL, Bcast<float>{rhi}, wa0, wb0);
-      chunk_codes<BITS, SYM>(raw1, NZ, RL, Bcast<float>{rhi}, wa1, wb1);
+      chunk_codes<PB, SYM>(raw0, NZ, RL, Bcast<float>{rhi}, wa0, wb0);
+      chunk_codes<PB, SYM>(raw1, NZ, RL, Bcast<float>{rhi}, wa1, wb1);
       uint32_t diff = 0;
 #pragma unroll
-      for (int j = 0; j < BITS / 4; ++j) diff |= (wa0[j] ^ wb0[j]) | (wa1[j] ^ wb1[j]);
+      for (int j = 0; j < PB / 4; ++j) diff |= (wa0[j] ^ wb0[j]) | (wa1[j] ^ wb1[j]);
       if (__any_sync(kFull, diff != 0)) {
-        settle_chunk<BITS, SYM>(wa0, wb0, xat0, zat, sat, rat);
-        settle_chunk<BITS, SYM>(wa1, wb1, xat1, zat, sat, rat);
+        settle_chunk<PB, SYM>(wa0, wb0, xat0, zat, sat, rat);
+        settle_chunk<PB, SYM>(wa1, wb1, xat1, zat, sat, rat);
       }
     } else {
-      slow_chunk<BITS, SYM>(wa0, xat0, zat, sat);
-      slow_chunk<BITS, SYM>(wa1, xat1, zat, sat);
+      slow_chunk<PB, SYM, kLev>(wa0, xat0, zat, sat);
+      slow_chunk<PB, SYM, kLev>(wa1, xat1, zat, sat);
     }
-    if (live) {
+    if (BITS == 3) {
+      // ten codes per word: through this warp's row buffer (one byte per code)
+      unsigned char* rb = rowbuf + rr * kHeadDim;
+      *reinterpret_cast<uint2*>(rb + 8 * c0) = make_uint2(wa0[0], wa0[PB / 4 - 1]);
+      *reinterpret_cast<uint2*>(rb + 8 * c1) = make_uint2(wa1[0], wa1[PB / 4 - 1]);
+      __syncwarp();
+      if (live) {
+        uint32_t* rowdst = T.codes + (int64_t)n * T.codes_sstride + (int64_t)(row0 + lr) * kWords;
+        rowdst[q] = pack3_word(rb, q);
+        if (q + 8 < kWords) rowdst[q + 8] = pack3_word(rb, q + 8);
+      }
+      __syncwarp();
+    } else if (live) {
       uint32_t* rowdst = T.codes + (int64_t)n * T.codes_sstride + (int64_t)(row0 + lr) * kWords;
       if (BITS == 4) {
         reinterpret_cast<uint2*>(rowdst)[q] = sw ? make_uint2(wa1[0], wa0[0]) : make_uint2(wa0[0], wa1[0]);
@@ -354,11 +385,13 @@ struct KeyScratch {
 
 template <int BITS, int TB>
 __device__ __forceinline__ bool key_block(const unsigned char* tile, const TensorDev& K, int n,
-                                          int blk, bool ok, KeyScratch& ks, int warp, int lane) {
+                                          int blk, bool ok, KeyScratch& ks, int warp, int lane,
+                                          unsigned char* rowbuf) {
   constexpr int kLev = (1 << BITS) - 1;
   constexpr int kRW = TB / kWarps;  // rows of this warp
   constexpr int kIt = kRW / 2;      // rows per lane
-  constexpr int kWords = 128 * BITS / 32;
+  constexpr int kWords = Pack<BITS>::kWords;
+  constexpr int PB = BITS == 3 ? 8 : BITS;
   const int o = lane & 15, p = lane >> 4;
   const uint4* t4 = reinterpret_cast<const uint4*>(tile);
   const __half2 pinf = __half2half2(__ushort_as_half(0x7C00));
@@ -439,17 +472,24 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
     const int row = warp * kRW + 2 * i + p;
     const uint4 raw = t4[row * 16 + o];
     auto xat = [&](int e) { return xs[row * kHeadDim + 8 * o + e]; };
-    uint32_t wa[BITS / 4], wb[BITS / 4];
+    uint32_t wa[PB / 4], wb[PB / 4];
     if (all_fast) {
-      chunk_codes<BITS, false>(raw, nz, rl, rh, wa, wb);
+      chunk_codes<PB, false>(raw, nz, rl, rh, wa, wb);
       uint32_t diff = 0;
 #pragma unroll
-      for (int j = 0; j < BITS / 4; ++j) diff |= wa[j] ^ wb[j];
-      if (__any_sync(kFull, diff != 0)) settle_chunk<BITS, false>(wa, wb, xat, zat, sat, rat);
+      for (int j = 0; j < PB / 4; ++j) diff |= wa[j] ^ wb[j];
+      if (__any_sync(kFull, diff != 0)) settle_chunk<PB, false>(wa, wb, xat, zat, sat, rat);
     } else {
-      slow_chunk<BITS, false>(wa, xat, zat, sat);
+      slow_chunk<PB, false, kLev>(wa, xat, zat, sat);
     }
-    if (BITS == 4)
+    if (BITS == 3) {
+      // ten codes per word: the two rows of this step through the row buffer
+      unsigned char* rb = rowbuf + p * kHeadDim;
+      *reinterpret_cast<uint2*>(rb + 8 * o) = make_uint2(wa[0], wa[PB / 4 - 1]);
+      __syncwarp();
+      if (o < kWords) kdst[(int64_t)row * kWords + o] = pack3_word(rb, o);
+      __syncwarp();
+    } else if (BITS == 4)
       kdst[(int64_t)row * kWords + o] = wa[0];
     else
       reinterpret_cast<uint2*>(kdst + (int64_t)row * kWords)[o] = make_uint2(wa[0], wa[1]);
@@ -472,25 +512,27 @@ struct Args {
   uint32_t* status;
 };
 
-template <int KB, int KMODE, int TB>
+template <int KB, int KMODE, int TB, int VB>
 struct Geo {
   static constexpr bool kPerChannel = KMODE == KVQ_ASYM_PER_CHANNEL;
   static constexpr int kRows = (kPerChannel && TB > 64) ? TB : 64;  // rows per item
   static constexpr int kStageBytes = kRows * kHeadDim * 2;
   static constexpr int kStages = kStageBytes <= 16384 ? 3 : 2;
   static constexpr size_t kScratch = kPerChannel ? sizeof(KeyScratch) : 0;
+  static constexpr size_t kRowBuf = (KB == 3 || VB == 3) ? 4 * kHeadDim : 0;  // per warp, 3-bit repacking
   static constexpr size_t kCtl = 64;  // counters and barriers
-  static constexpr size_t kBytes = (size_t)kStages * kStageBytes + kScratch + kCtl;
+  static constexpr size_t kBytes = (size_t)kStages * kStageBytes + kScratch + kWarps * kRowBuf + kCtl;
 };
 
 template <int KB, int KMODE, int TB, int VB, bool VSYM>
 __global__ void __launch_bounds__(kThreads, 4) prefill_fast_kernel(Args a) {
-  using G = Geo<KB, KMODE, TB>;
+  using G = Geo<KB, KMODE, TB, VB>;
   constexpr int S = G::kStages;
   constexpr int RPW = G::kRows / kWarps;
   extern __shared__ __align__(128) unsigned char smem[];
   KeyScratch& ks = *reinterpret_cast<KeyScratch*>(smem + S * G::kStageBytes);
-  unsigned char* ctl = smem + S * G::kStageBytes + G::kScratch;
+  unsigned char* rowbuf = smem + S * G::kStageBytes + G::kScratch + (size_t)(threadIdx.x >> 5) * G::kRowBuf;
+  unsigned char* ctl = smem + S * G::kStageBytes + G::kScratch + kWarps * G::kRowBuf;
   int* cnt = reinterpret_cast<int*>(ctl);           // [S] warps done with a stage
   int* issued = reinterpret_cast<int*>(ctl + 16);   // [S] copies issued into a stage
   uint64_t* full = reinterpret_cast<uint64_t*>(ctl + 32);  // [S]
@@ -562,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 4) prefill_fast_kernel(Args a) {
     const unsigned char* tile = smem + (size_t)s * G::kStageBytes;
     if (r.kind == 0) {
       if constexpr (G::kPerChannel) {
-        if (!key_block<KB, TB>(tile, a.k, r.n, r.idx, ok, ks, warp, lane)) dead = true;
+        if (!key_block<KB, TB>(tile, a.k, r.n, r.idx, ok, ks, warp, lane, rowbuf)) dead = true;
       }
     } else if (!dead) {
       if (r.kind == 1) {
@@ -573,9 +615,9 @@ __global__ void __launch_bounds__(kThreads, 4) prefill_fast_kernel(Args a) {
         const int count = (a.seq_len - t0) * (kHeadDim / 8);
         for (int i = tid; i < count; i += kThreads) d4[i] = s4[i];
       } else if (r.kind == 2) {
-        rows_warp<KB, KMODE == KVQ_SYM_PER_TOKEN, RPW>(tile, a.k, r.n, r.row0, r.nrows, warp, lane);
+        rows_warp<KB, KMODE == KVQ_SYM_PER_TOKEN, RPW>(tile, a.k, r.n, r.row0, r.nrows, warp, lane, rowbuf);
       } else {
-        rows_warp<VB, VSYM, RPW>(tile, a.v, r.n, r.row0, r.nrows, warp, lane);
+        rows_warp<VB, VSYM, RPW>(tile, a.v, r.n, r.row0, r.nrows, warp, lane, rowbuf);
       }
     }
     if (!dead) {
@@ -606,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 4) prefill_fast_kernel(Args a) {
 template <int KB, int KMODE, int TB, int VB, bool VSYM>
 cudaError_t launch_fast_t(const LayerDev& L, const __half* k, const __half* v, int seq_len,
                           cudaStream_t st) {
-  using G = Geo<KB, KMODE, TB>;
+  using G = Geo<KB, KMODE, TB, VB>;
   auto kern = prefill_fast_kernel<KB, KMODE, TB, VB, VSYM>;
   static int occ = 0;
   if (occ == 0) {

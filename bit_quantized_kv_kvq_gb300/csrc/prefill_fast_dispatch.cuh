@@ -1,5 +1,5 @@
-// Dispatch of the prefill kernels without outliers and with 4- or 8-bit
-// codes (prefill_fast.cuh) for one value codec, chosen by the including
+// Dispatch of the prefill kernels without outliers (prefill_fast.cuh) for
+// one value codec, chosen by the including
 // translation unit through KVQ_PF_VB and KVQ_PF_VSYM.
 #pragma once
 #include "prefill_fast.cuh"
@@ -18,17 +18,20 @@ cudaError_t KVQ_PF_NAME(KVQ_PF_VB, KVQ_PF_VSYM)(const LayerDev& L, const __half*
   constexpr int VB = KVQ_PF_VB;
   constexpr bool VS = KVQ_PF_VSYM != 0;
   const TensorDev& K = L.k;
-  if (K.mode == KVQ_ASYM_PER_CHANNEL) {
-    if (K.bits == 4) {
-      if (K.group == 64) return pfx::launch_fast_t<4, KVQ_ASYM_PER_CHANNEL, 64, VB, VS>(L, k, v, seq_len, st);
-      return pfx::launch_fast_t<4, KVQ_ASYM_PER_CHANNEL, 128, VB, VS>(L, k, v, seq_len, st);
-    }
-    if (K.group == 64) return pfx::launch_fast_t<8, KVQ_ASYM_PER_CHANNEL, 64, VB, VS>(L, k, v, seq_len, st);
-    return pfx::launch_fast_t<8, KVQ_ASYM_PER_CHANNEL, 128, VB, VS>(L, k, v, seq_len, st);
+#define KVQ_PF_KB(B)                                                                               \
+  if (K.bits == B) {                                                                               \
+    if (K.mode == KVQ_ASYM_PER_CHANNEL) {                                                          \
+      if (K.group == 64) return pfx::launch_fast_t<B, KVQ_ASYM_PER_CHANNEL, 64, VB, VS>(L, k, v, seq_len, st); \
+      return pfx::launch_fast_t<B, KVQ_ASYM_PER_CHANNEL, 128, VB, VS>(L, k, v, seq_len, st);     \
+    }                                                                                              \
+    return pfx::launch_fast_t<B, KVQ_ASYM_PER_TOKEN, 1, VB, VS>(L, k, v, seq_len, st);           \
   }
   if (K.mode == KVQ_SYM_PER_TOKEN) return pfx::launch_fast_t<8, KVQ_SYM_PER_TOKEN, 1, VB, VS>(L, k, v, seq_len, st);
-  if (K.bits == 4) return pfx::launch_fast_t<4, KVQ_ASYM_PER_TOKEN, 1, VB, VS>(L, k, v, seq_len, st);
-  return pfx::launch_fast_t<8, KVQ_ASYM_PER_TOKEN, 1, VB, VS>(L, k, v, seq_len, st);
+  KVQ_PF_KB(3)
+  KVQ_PF_KB(4)
+  KVQ_PF_KB(8)
+#undef KVQ_PF_KB
+  return cudaErrorNotSupported;
 }
 
 }  // namespace kvq

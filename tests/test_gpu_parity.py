@@ -203,6 +203,12 @@ NO_OUTLIER_CODECS = [
                          k_group=16, v_group=16)),
     ("q8_g64", dict(k_bits=8, v_bits=8, k_mode=W.SYM_PER_TOKEN, v_mode=W.SYM_PER_TOKEN,
                     k_group=64, v_group=64)),
+    ("k3c64_v3g128", dict(k_bits=3, v_bits=3, k_mode=W.ASYM_PER_CHANNEL, v_mode=W.ASYM_PER_TOKEN,
+                          k_group=64, v_group=128)),
+    ("k3t128_v4g64", dict(k_bits=3, v_bits=4, k_mode=W.ASYM_PER_TOKEN, v_mode=W.ASYM_PER_TOKEN,
+                          k_group=128, v_group=64)),
+    ("k8c64_v3g128", dict(k_bits=8, v_bits=3, k_mode=W.ASYM_PER_CHANNEL, v_mode=W.ASYM_PER_TOKEN,
+                          k_group=64, v_group=128)),
 ]
 
 
