@@ -237,6 +237,147 @@ __device__ __forceinline__ void slow_chunk(uint32_t (&wa)[BITS / 4], XAt x_at, Z
   }
 }
 
+// ---------------------------------------------------------------------------
+// Outliers (KVQuant page, cf-1.com/news/2306543, §2.2 item 3): the k largest
+// |x| of a (token, head) row, ties to the lower channel, stored as CSR sorted
+// by channel; their slots are left out of the group statistics and get code
+// 0.
+//
+// Selection works on packed fp16 magnitudes (sign bits cleared; for
+// non-negative halves the fp16 order is the order of |x|). Round r takes
+// M_r = max{|x| : |x| < M_(r-1)} over the row (lanes reduce by shuffles);
+// after k rounds the slots with |x| >= M_k are the outliers exactly when
+// there are k of them. Otherwise a magnitude repeats at the top of the row
+// (a tie), and the warp redoes the selection with unique keys
+// (|x| bits << 16) | (128 - channel): round r then takes the largest key
+// below the one round r-1 took.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t hmax2_bits(uint32_t a, uint32_t b) {
+  const __half2 r = __hmax2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t ge_mask(uint32_t a, uint32_t b) {
+  return __hge2_mask(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+}
+__device__ __forceinline__ uint32_t lt_mask(uint32_t a, uint32_t b) {
+  return __hlt2_mask(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+}
+
+// Maximum over NP packed pairs of this lane and the NL lanes of its row
+// (xor 1 .. NL/2), in both halves of the result.
+template <int NP, int NL>
+__device__ __forceinline__ uint32_t row_max2(const uint32_t (&v)[NP]) {
+  uint32_t m = v[0];
+#pragma unroll
+  for (int p = 1; p < NP; ++p) m = hmax2_bits(m, v[p]);
+  m = hmax2_bits(m, __byte_perm(m, 0u, 0x1032u));
+#pragma unroll
+  for (int off = 1; off < NL; off <<= 1) m = hmax2_bits(m, __shfl_xor_sync(kFull, m, off));
+  return m;
+}
+
+// M_k of the row (k >= 1) from the magnitudes a of this lane's pairs.
+template <int NP, int NL>
+__device__ __forceinline__ uint32_t kth_magnitude(const uint32_t (&a)[NP], int kout) {
+  uint32_t m = row_max2<NP, NL>(a);
+  for (int r = 1; r < kout; ++r) {
+    uint32_t b[NP];
+#pragma unroll
+    for (int p = 0; p < NP; ++p) b[p] = a[p] & lt_mask(a[p], m);
+    m = row_max2<NP, NL>(b);
+  }
+  return m;
+}
+
+// Bits of NP pair masks (0xFFFF per selected half): element 2p <- bit 2p,
+// element 2p + 1 <- bit 2p + 1.
+template <int NP>
+__device__ __forceinline__ uint32_t mask_bits(const uint32_t (&mk)[NP]) {
+  uint32_t b = 0;
+#pragma unroll
+  for (int p = 0; p < NP; ++p) b |= (mk[p] & 0x00010001u) << (2 * p);
+  return (b | (b >> 15)) & ((1u << (2 * NP)) - 1u);
+}
+
+// Pair masks of four pairs from eight element bits (the inverse of
+// mask_bits): bits 2p and 2p + 1 are moved to the sign bits of bytes 0 and 1
+// and replicated by a sign-extending byte permute.
+__device__ __forceinline__ void expand_mask4(uint32_t bits, uint32_t (&mk)[4]) {
+  const uint32_t t = bits | (bits << 7);  // bit i (i < 8) at i and i + 7
+#pragma unroll
+  for (int p = 0; p < 4; ++p) {
+    // selector nibbles 8, 8, 9, 9: bytes 0 and 1 of the result take the sign
+    // of source byte 0, bytes 2 and 3 the sign of source byte 1
+    asm("prmt.b32 %0, %1, 0, 0x9988;" : "=r"(mk[p]) : "r"(t << (7 - 2 * p)));
+  }
+}
+
+__device__ __forceinline__ uint32_t outlier_key(uint16_t xh, int ch) {
+  return ((uint32_t)(xh & 0x7FFFu) << 16) | (uint32_t)(kHeadDim - ch);
+}
+
+// k rounds of the keyed max over a group of NL lanes (xor 1 .. NL/2);
+// returns the key of the k-th largest |x| of the row.
+template <int NL, int NE>
+__device__ __forceinline__ uint32_t kth_key(const uint32_t (&key)[NE], int kout) {
+  uint32_t thr = 0xFFFFFFFFu;
+  for (int r = 0; r < kout; ++r) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < NE; ++i) m = max(m, key[i] < thr ? key[i] : 0u);
+#pragma unroll
+    for (int off = 1; off < NL; off <<= 1) m = max(m, __shfl_xor_sync(kFull, m, off));
+    thr = m;
+  }
+  return thr;
+}
+
+// CSR entries of this lane's outliers (om: bit i <- channel ch0 + i, in
+// channel order) at positions first, first + 1, ... of the row; xs holds the
+// row's fp16 values.
+__device__ __forceinline__ void write_lane_csr(const TensorDev& T, int n, int row, int kout,
+                                               uint32_t om, int ch0, int first,
+                                               const uint16_t* xs) {
+  const int64_t base = (int64_t)n * T.out_sstride + (int64_t)row * kout + first;
+  int i = 0;
+  for (uint32_t m = om; m; m &= m - 1, ++i) {
+    const int c = ch0 + __ffs(m) - 1;
+    T.col[base + i] = (uint16_t)c;
+    T.val[base + i] = __ushort_as_half(xs[c]);
+  }
+}
+
+__device__ __forceinline__ void write_rowptr(const TensorDev& T, int n, int row, int kout) {
+  int32_t* rp = T.rowptr + (int64_t)n * T.rowptr_sstride;
+  rp[row + 1] = (row + 1) * kout;
+  if (row == 0) rp[0] = 0;
+}
+
+// Exclusive prefix sum of v over the NL lanes of a row, and the row total.
+template <int NL>
+__device__ __forceinline__ int row_scan(int v, int li, int& total) {
+  int s = v;
+#pragma unroll
+  for (int d = 1; d < NL; d <<= 1) {
+    const int t = __shfl_up_sync(kFull, s, d, NL);
+    if (li >= d) s += t;
+  }
+  total = __shfl_sync(kFull, s, NL - 1, NL);
+  return s - v;
+}
+
+// Clears field i (of PB bits) of an eight-code chunk packed in w.
+template <int PB>
+__device__ __forceinline__ void clear_field(uint32_t (&w)[PB / 4], int i) {
+  if (PB == 4) {
+    w[0] = bfi(0u, w[0], (uint32_t)(4 * i), 4);
+  } else if (i < 4) {
+    w[0] = bfi(0u, w[0], (uint32_t)(8 * i), 8);
+  } else {
+    w[PB / 4 - 1] = bfi(0u, w[PB / 4 - 1], (uint32_t)(8 * (i - 4)), 8);
+  }
+}
+
 // Word w (ten 3-bit codes, top two bits zero; word 12 holds eight) of a row
 // whose 128 codes sit one per byte in shared memory (16-byte aligned).
 __device__ __forceinline__ uint32_t pack3_word(const unsigned char* row, int w) {
@@ -259,10 +400,10 @@ __device__ __forceinline__ uint32_t pack3_word(const unsigned char* row, int w) 
 // code one row (16 channels each: 16-byte chunks 2q and 2q + 1, read in an
 // order that keeps the four rows of a warp instruction on distinct banks).
 // ---------------------------------------------------------------------------
-template <int BITS, bool SYM, int RPW>
+template <int BITS, bool SYM, int RPW, bool OUTL>
 __device__ __forceinline__ void rows_warp(const unsigned char* tile, const TensorDev& T, int n,
                                           int row0, int nrows, int warp, int lane,
-                                          unsigned char* rowbuf) {
+                                          unsigned char* rowbuf, int kout) {
   constexpr int kLev = SYM ? (1 << (BITS - 1)) - 1 : (1 << BITS) - 1;
   constexpr int kWords = Pack<BITS>::kWords;
   constexpr int PB = BITS == 3 ? 8 : BITS;  // field width while coding (3-bit codes go one per byte)
@@ -276,7 +417,57 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
     const bool live = lr < nrows;
     const uint4* rowp = reinterpret_cast<const uint4*>(tile + (size_t)lr * (kHeadDim * 2));
     const int c0 = 2 * q + sw, c1 = 2 * q + 1 - sw;  // chunk indices of raw0, raw1
-    const uint4 raw0 = rowp[c0], raw1 = rowp[c1];
+    uint4 raw0 = rowp[c0], raw1 = rowp[c1];
+    // outliers: om0 / om1 bit e <- element e of chunk c0 / c1; mk[p] the
+    // mask of pair p (pairs 0-3 of raw0, 4-7 of raw1)
+    uint32_t om0 = 0, om1 = 0, mk[8];
+    if (OUTL) {
+      const uint32_t wv[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
+      uint32_t a[8];
+#pragma unroll
+      for (int p = 0; p < 8; ++p) a[p] = wv[p] & 0x7FFF7FFFu;
+      const uint32_t mk_th = kth_magnitude<8, 8>(a, kout);
+#pragma unroll
+      for (int p = 0; p < 8; ++p) mk[p] = ge_mask(a[p], mk_th);
+      om0 = mask_bits<4>(*reinterpret_cast<const uint32_t(*)[4]>(&mk[0]));
+      om1 = mask_bits<4>(*reinterpret_cast<const uint32_t(*)[4]>(&mk[4]));
+      int total;
+      int first = row_scan<8>(__popc(om0) + __popc(om1), q, total);
+      if (__any_sync(kFull, total != kout)) {
+        // a repeated magnitude at the top of some row: unique keys
+        const uint16_t* hx0 = reinterpret_cast<const uint16_t*>(&raw0);
+        const uint16_t* hx1 = reinterpret_cast<const uint16_t*>(&raw1);
+        uint32_t key[16];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          key[e] = outlier_key(hx0[e], 8 * c0 + e);
+          key[8 + e] = outlier_key(hx1[e], 8 * c1 + e);
+        }
+        const uint32_t kw = kth_key<8, 16>(key, kout);
+        om0 = 0;
+        om1 = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          om0 |= (key[e] >= kw ? 1u : 0u) << e;
+          om1 |= (key[8 + e] >= kw ? 1u : 0u) << e;
+        }
+        expand_mask4(om0, *reinterpret_cast<uint32_t(*)[4]>(&mk[0]));
+        expand_mask4(om1, *reinterpret_cast<uint32_t(*)[4]>(&mk[4]));
+        first = row_scan<8>(__popc(om0) + __popc(om1), q, total);
+      }
+      if (live) {
+        const uint16_t* xs = reinterpret_cast<const uint16_t*>(rowp);
+        const uint32_t om16 = sw ? (om1 | (om0 << 8)) : (om0 | (om1 << 8));  // channel order
+        write_lane_csr(T, n, row0 + lr, kout, om16, 16 * q, first, xs);
+        if (q == 0) write_rowptr(T, n, row0 + lr, kout);
+      }
+      if (SYM) {
+        // an outlier slot reads +0: the absolute maximum of the rest stays,
+        // and the slot codes 0
+        raw0 = make_uint4(wv[0] & ~mk[0], wv[1] & ~mk[1], wv[2] & ~mk[2], wv[3] & ~mk[3]);
+        raw1 = make_uint4(wv[4] & ~mk[4], wv[5] & ~mk[5], wv[6] & ~mk[6], wv[7] & ~mk[7]);
+      }
+    }
     const __half2* h0 = reinterpret_cast<const __half2*>(&raw0);
     const __half2* h1 = reinterpret_cast<const __half2*>(&raw1);
     float s, nz = 0.0f, rlo, rhi;
@@ -297,11 +488,27 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
       s16 = __float2half_rn(div_levels<kLev>(am));
       z16 = __ushort_as_half(0);
     } else {
-      __half2 mn = __hmin2(h0[0], h0[1]), mx = __hmax2(h0[0], h0[1]);
-      mn = __hmin2(mn, __hmin2(h0[2], h0[3]));
-      mx = __hmax2(mx, __hmax2(h0[2], h0[3]));
-      mn = __hmin2(mn, __hmin2(__hmin2(h1[0], h1[1]), __hmin2(h1[2], h1[3])));
-      mx = __hmax2(mx, __hmax2(__hmax2(h1[0], h1[1]), __hmax2(h1[2], h1[3])));
+      __half2 vn[8], vx[8];
+#pragma unroll
+      for (int p = 0; p < 8; ++p) {
+        const __half2 h = p < 4 ? h0[p] : h1[p - 4];
+        if (OUTL) {
+          // outlier slots read +inf for the minimum and -inf for the maximum
+          const uint32_t w = *reinterpret_cast<const uint32_t*>(&h);
+          const uint32_t wn = (w & ~mk[p]) | (0x7C007C00u & mk[p]);
+          const uint32_t wx = (w & ~mk[p]) | (0xFC00FC00u & mk[p]);
+          vn[p] = *reinterpret_cast<const __half2*>(&wn);
+          vx[p] = *reinterpret_cast<const __half2*>(&wx);
+        } else {
+          vn[p] = h;
+          vx[p] = h;
+        }
+      }
+      __half2 mn = __hmin2(vn[0], vn[1]), mx = __hmax2(vx[0], vx[1]);
+      mn = __hmin2(mn, __hmin2(vn[2], vn[3]));
+      mx = __hmax2(mx, __hmax2(vx[2], vx[3]));
+      mn = __hmin2(mn, __hmin2(__hmin2(vn[4], vn[5]), __hmin2(vn[6], vn[7])));
+      mx = __hmax2(mx, __hmax2(__hmax2(vx[4], vx[5]), __hmax2(vx[6], vx[7])));
       const __half2 nmx = __hneg2(mx);
       __half2 pr = __hmin2(__lows2half2(mn, nmx), __highs2half2(mn, nmx));  // (min, -max)
       for (int off = 1; off < lpg; off <<= 1) {
@@ -314,6 +521,17 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
       s16 = __float2half_rn(div_levels<kLev>(__fsub_rn(mxv, mnv)));
       z16 = __float2half_rn(mnv);
       nz = -mnv;
+      if (OUTL) {
+        // an outlier slot codes the zero point: d = 0, code 0
+        const uint32_t z2 = (uint32_t)__half_as_ushort(z16) * 0x10001u;
+        uint32_t* r0 = reinterpret_cast<uint32_t*>(&raw0);
+        uint32_t* r1 = reinterpret_cast<uint32_t*>(&raw1);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+          r0[p] = (r0[p] & ~mk[p]) | (z2 & mk[p]);
+          r1[p] = (r1[p] & ~mk[4 + p]) | (z2 & mk[4 + p]);
+        }
+      }
     }
     s = __half2float(s16);
     scale_bracket(s, rlo, rhi, slow);
@@ -346,6 +564,10 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
     } else {
       slow_chunk<PB, SYM, kLev>(wa0, xat0, zat, sat);
       slow_chunk<PB, SYM, kLev>(wa1, xat1, zat, sat);
+      if (OUTL) {  // the IEEE path coded the outliers' own values
+        for (uint32_t m = om0; m; m &= m - 1) clear_field<PB>(wa0, __ffs(m) - 1);
+        for (uint32_t m = om1; m; m &= m - 1) clear_field<PB>(wa1, __ffs(m) - 1);
+      }
     }
     if (BITS == 3) {
       // ten codes per word: through this warp's row buffer (one byte per code)
@@ -383,10 +605,10 @@ struct KeyScratch {
   float nz[kHeadDim], rlo[kHeadDim], rhi[kHeadDim], s[kHeadDim];
 };
 
-template <int BITS, int TB>
+template <int BITS, int TB, bool OUTL>
 __device__ __forceinline__ bool key_block(const unsigned char* tile, const TensorDev& K, int n,
                                           int blk, bool ok, KeyScratch& ks, int warp, int lane,
-                                          unsigned char* rowbuf) {
+                                          unsigned char* rowbuf, int kout, uint8_t* ombuf) {
   constexpr int kLev = (1 << BITS) - 1;
   constexpr int kRW = TB / kWarps;  // rows of this warp
   constexpr int kIt = kRW / 2;      // rows per lane
@@ -404,12 +626,54 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
   }
 #pragma unroll 4
   for (int i = 0; i < kIt; ++i) {
-    const uint4 raw = t4[(warp * kRW + 2 * i + p) * 16 + o];
+    const int row = warp * kRW + 2 * i + p;
+    const uint4 raw = t4[row * 16 + o];
     const __half2* h = reinterpret_cast<const __half2*>(&raw);
+    if (OUTL) {
+      // outliers of token row `row` (sixteen lanes hold it), left out of the
+      // per-channel statistics; the lane's bits are kept for the code pass
+      const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t a[4], mk[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      mn[j] = __hmin2(mn[j], h[j]);
-      mx[j] = __hmax2(mx[j], h[j]);
+      for (int j = 0; j < 4; ++j) a[j] = wv[j] & 0x7FFF7FFFu;
+      const uint32_t th = kth_magnitude<4, 16>(a, kout);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mk[j] = ge_mask(a[j], th);
+      uint32_t om = mask_bits<4>(mk);
+      int total;
+      int first = row_scan<16>(__popc(om), o, total);
+      if (__any_sync(kFull, total != kout)) {
+        // a repeated magnitude at the top of some row: unique keys
+        const uint16_t* hx = reinterpret_cast<const uint16_t*>(&raw);
+        uint32_t key[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) key[e] = outlier_key(hx[e], 8 * o + e);
+        const uint32_t kw = kth_key<16, 8>(key, kout);
+        om = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) om |= (key[e] >= kw ? 1u : 0u) << e;
+        expand_mask4(om, mk);
+        first = row_scan<16>(__popc(om), o, total);
+      }
+      if (ok) {
+        write_lane_csr(K, n, blk * TB + row, kout, om, 8 * o, first,
+                       reinterpret_cast<const uint16_t*>(tile + (size_t)row * kHeadDim * 2));
+        if (o == 0) write_rowptr(K, n, blk * TB + row, kout);
+      }
+      ombuf[i * 32 + lane] = (uint8_t)om;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t wn = (wv[j] & ~mk[j]) | (0x7C007C00u & mk[j]);  // +inf
+        const uint32_t wx = (wv[j] & ~mk[j]) | (0xFC00FC00u & mk[j]);  // -inf
+        mn[j] = __hmin2(mn[j], *reinterpret_cast<const __half2*>(&wn));
+        mx[j] = __hmax2(mx[j], *reinterpret_cast<const __half2*>(&wx));
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        mn[j] = __hmin2(mn[j], h[j]);
+        mx[j] = __hmax2(mx[j], h[j]);
+      }
     }
   }
 #pragma unroll
@@ -434,8 +698,12 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
       m0 = __hmin(m0, ks.mn[w][c]);
       m1 = __hmax(m1, ks.mx[w][c]);
     }
-    const float mnv = __fadd_rn(__half2float(m0), 0.0f);
-    const float mxv = __fadd_rn(__half2float(m1), 0.0f);
+    float mnv = __fadd_rn(__half2float(m0), 0.0f);
+    float mxv = __fadd_rn(__half2float(m1), 0.0f);
+    if (OUTL && mnv > mxv) {  // every member of the channel's block is an outlier
+      mnv = 0.0f;
+      mxv = 0.0f;
+    }
     const __half s16 = __float2half_rn(div_levels<kLev>(__fsub_rn(mxv, mnv)));
     const __half z16 = __float2half_rn(mnv);
     reinterpret_cast<__half2*>(K.meta + (int64_t)n * K.meta_sstride)[(int64_t)blk * kHeadDim + c] =
@@ -462,6 +730,11 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
     rl[4 * j] = b.x; rl[4 * j + 1] = b.y; rl[4 * j + 2] = b.z; rl[4 * j + 3] = b.w;
     rh[4 * j] = c.x; rh[4 * j + 1] = c.y; rh[4 * j + 2] = c.z; rh[4 * j + 3] = c.w;
   }
+  uint32_t zh[4];  // the zero points of this lane's channel pairs, fp16 (exact)
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    zh[j] = (uint32_t)__half_as_ushort(__float2half_rn(-nz[2 * j])) |
+            ((uint32_t)__half_as_ushort(__float2half_rn(-nz[2 * j + 1])) << 16);
   uint32_t* kdst = K.codes + (int64_t)n * K.codes_sstride + (int64_t)blk * TB * kWords;
   const uint16_t* xs = reinterpret_cast<const uint16_t*>(tile);
   auto zat = [&](int i) { return ks.nz[8 * o + i]; };
@@ -470,9 +743,21 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
 #pragma unroll 2
   for (int i = 0; i < kIt; ++i) {
     const int row = warp * kRW + 2 * i + p;
-    const uint4 raw = t4[row * 16 + o];
+    uint4 raw = t4[row * 16 + o];
     auto xat = [&](int e) { return xs[row * kHeadDim + 8 * o + e]; };
     uint32_t wa[PB / 4], wb[PB / 4];
+    const uint32_t om = OUTL ? ombuf[i * 32 + lane] : 0u;
+    if (OUTL) {
+      // an outlier slot codes its channel's zero point (code 0 in both
+      // brackets): its own value may lie outside the range, and a field out
+      // of range would carry into its neighbours when the fields are summed
+      uint32_t mk[4];
+      expand_mask4(om, mk);
+      raw.x = (raw.x & ~mk[0]) | (zh[0] & mk[0]);
+      raw.y = (raw.y & ~mk[1]) | (zh[1] & mk[1]);
+      raw.z = (raw.z & ~mk[2]) | (zh[2] & mk[2]);
+      raw.w = (raw.w & ~mk[3]) | (zh[3] & mk[3]);
+    }
     if (all_fast) {
       chunk_codes<PB, false>(raw, nz, rl, rh, wa, wb);
       uint32_t diff = 0;
@@ -481,6 +766,8 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
       if (__any_sync(kFull, diff != 0)) settle_chunk<PB, false>(wa, wb, xat, zat, sat, rat);
     } else {
       slow_chunk<PB, false, kLev>(wa, xat, zat, sat);
+      if (OUTL)
+        for (uint32_t m = om; m; m &= m - 1) clear_field<PB>(wa, __ffs(m) - 1);
     }
     if (BITS == 3) {
       // ten codes per word: the two rows of this step through the row buffer
@@ -509,10 +796,11 @@ struct Args {
   int k_nfull;  // whole per-channel key blocks per stream
   int v_items;  // value row chunks per stream
   int n_streams;
+  int kout;  // outliers per row (0: none)
   uint32_t* status;
 };
 
-template <int KB, int KMODE, int TB, int VB>
+template <int KB, int KMODE, int TB, int VB, bool OUTL>
 struct Geo {
   static constexpr bool kPerChannel = KMODE == KVQ_ASYM_PER_CHANNEL;
   static constexpr int kRows = (kPerChannel && TB > 64) ? TB : 64;  // rows per item
@@ -520,19 +808,23 @@ struct Geo {
   static constexpr int kStages = kStageBytes <= 16384 ? 3 : 2;
   static constexpr size_t kScratch = kPerChannel ? sizeof(KeyScratch) : 0;
   static constexpr size_t kRowBuf = (KB == 3 || VB == 3) ? 4 * kHeadDim : 0;  // per warp, 3-bit repacking
+  // per warp, the outlier masks of its key-block rows between the two passes
+  static constexpr size_t kOmBuf = (kPerChannel && OUTL) ? (size_t)TB / 8 * 32 : 0;
   static constexpr size_t kCtl = 64;  // counters and barriers
-  static constexpr size_t kBytes = (size_t)kStages * kStageBytes + kScratch + kWarps * kRowBuf + kCtl;
+  static constexpr size_t kBytes =
+      (size_t)kStages * kStageBytes + kScratch + kWarps * (kRowBuf + kOmBuf) + kCtl;
 };
 
-template <int KB, int KMODE, int TB, int VB, bool VSYM>
+template <int KB, int KMODE, int TB, int VB, bool VSYM, bool OUTL>
 __global__ void __launch_bounds__(kThreads, 4) prefill_fast_kernel(Args a) {
-  using G = Geo<KB, KMODE, TB, VB>;
+  using G = Geo<KB, KMODE, TB, VB, OUTL>;
   constexpr int S = G::kStages;
   constexpr int RPW = G::kRows / kWarps;
   extern __shared__ __align__(128) unsigned char smem[];
   KeyScratch& ks = *reinterpret_cast<KeyScratch*>(smem + S * G::kStageBytes);
   unsigned char* rowbuf = smem + S * G::kStageBytes + G::kScratch + (size_t)(threadIdx.x >> 5) * G::kRowBuf;
-  unsigned char* ctl = smem + S * G::kStageBytes + G::kScratch + kWarps * G::kRowBuf;
+  uint8_t* ombuf = smem + S * G::kStageBytes + G::kScratch + kWarps * G::kRowBuf + (size_t)(threadIdx.x >> 5) * G::kOmBuf;
+  unsigned char* ctl = smem + S * G::kStageBytes + G::kScratch + kWarps * (G::kRowBuf + G::kOmBuf);
   int* cnt = reinterpret_cast<int*>(ctl);           // [S] warps done with a stage
   int* issued = reinterpret_cast<int*>(ctl + 16);   // [S] copies issued into a stage
   uint64_t* full = reinterpret_cast<uint64_t*>(ctl + 32);  // [S]
@@ -604,7 +896,8 @@ __global__ void __launch_bounds__(kThreads, 4) prefill_fast_kernel(Args a) {
     const unsigned char* tile = smem + (size_t)s * G::kStageBytes;
     if (r.kind == 0) {
       if constexpr (G::kPerChannel) {
-        if (!key_block<KB, TB>(tile, a.k, r.n, r.idx, ok, ks, warp, lane, rowbuf)) dead = true;
+        if (!key_block<KB, TB, OUTL>(tile, a.k, r.n, r.idx, ok, ks, warp, lane, rowbuf, a.kout, ombuf))
+          dead = true;
       }
     } else if (!dead) {
       if (r.kind == 1) {
@@ -615,9 +908,10 @@ __global__ void __launch_bounds__(kThreads, 4) prefill_fast_kernel(Args a) {
         const int count = (a.seq_len - t0) * (kHeadDim / 8);
         for (int i = tid; i < count; i += kThreads) d4[i] = s4[i];
       } else if (r.kind == 2) {
-        rows_warp<KB, KMODE == KVQ_SYM_PER_TOKEN, RPW>(tile, a.k, r.n, r.row0, r.nrows, warp, lane, rowbuf);
+        rows_warp<KB, KMODE == KVQ_SYM_PER_TOKEN, RPW, OUTL>(tile, a.k, r.n, r.row0, r.nrows, warp, lane,
+                                                             rowbuf, a.kout);
       } else {
-        rows_warp<VB, VSYM, RPW>(tile, a.v, r.n, r.row0, r.nrows, warp, lane, rowbuf);
+        rows_warp<VB, VSYM, RPW, OUTL>(tile, a.v, r.n, r.row0, r.nrows, warp, lane, rowbuf, a.kout);
       }
     }
     if (!dead) {
@@ -645,11 +939,11 @@ __global__ void __launch_bounds__(kThreads, 4) prefill_fast_kernel(Args a) {
       if (issued[s] > 0) (void)mbar_wait_bounded(&full[s], (uint32_t)(issued[s] - 1) & 1u);
 }
 
-template <int KB, int KMODE, int TB, int VB, bool VSYM>
+template <int KB, int KMODE, int TB, int VB, bool VSYM, bool OUTL>
 cudaError_t launch_fast_t(const LayerDev& L, const __half* k, const __half* v, int seq_len,
                           cudaStream_t st) {
-  using G = Geo<KB, KMODE, TB, VB>;
-  auto kern = prefill_fast_kernel<KB, KMODE, TB, VB, VSYM>;
+  using G = Geo<KB, KMODE, TB, VB, OUTL>;
+  auto kern = prefill_fast_kernel<KB, KMODE, TB, VB, VSYM, OUTL>;
   static int occ = 0;
   if (occ == 0) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -666,6 +960,7 @@ cudaError_t launch_fast_t(const LayerDev& L, const __half* k, const __half* v, i
   a.vsrc = v;
   a.seq_len = seq_len;
   a.n_streams = L.n_streams;
+  a.kout = OUTL ? L.outliers : 0;
   a.status = L.status;
   a.v_items = (seq_len + G::kRows - 1) / G::kRows;
   if (G::kPerChannel) {

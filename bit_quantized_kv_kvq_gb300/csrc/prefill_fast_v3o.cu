@@ -1,0 +1,5 @@
+// Prefill kernels with the outlier split, values with 3-bit codes.
+#define KVQ_PF_VB 3
+#define KVQ_PF_VSYM 0
+#define KVQ_PF_OUTL 1
+#include "prefill_fast_dispatch.cuh"

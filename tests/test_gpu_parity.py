@@ -275,6 +275,61 @@ def test_exact_ties_and_tiny_scales(name, codec):
     assert cache.status() == 0
 
 
+def _outlier_inputs(wl, seed):
+    """Seeded K/V with rows that stress the top-k selection: a row of equal
+    magnitudes (ties go to the lower channel), a row of signed zeros, two
+    channels far above the rest over the first 128 tokens (every key block
+    there has channels whose members are all outliers), and a row whose
+    largest magnitudes occur with both signs."""
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(wl.seq_len)
+    g = torch.Generator().manual_seed(seed)
+    for x in (k, v):
+        sgn = torch.where(torch.rand(x.shape[-1], generator=g) < 0.5, -1.0, 1.0).to(x.dtype)
+        x[:, :, 5] = 0.75 * sgn
+        x[:, :, 6] = torch.where(torch.arange(x.shape[-1]) % 2 == 0, 0.0, -0.0).to(x.dtype)
+        x[:, :, :128, 17] = 100.0
+        x[:, :, :128, 90] = -100.0
+        x[:, :, 7, 3] = 9.0
+        x[:, :, 7, 40] = -9.0
+        x[:, :, 7, 41] = 9.0
+    return k, v
+
+
+@pytest.mark.parametrize("kout", [1, 3, 8])
+@pytest.mark.parametrize("seq", [65, 300])
+@pytest.mark.parametrize("name,codec", NO_OUTLIER_CODECS, ids=[c[0] for c in NO_OUTLIER_CODECS])
+def test_outlier_split_prefill(name, codec, seq, kout):
+    """The dense-and-sparse split at every supported codec: CSR lists, the
+    statistics over the remaining members and the zeroed outlier codes."""
+    wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=2, num_kv_heads=2, seq_len=seq,
+                 outliers_per_row=kout, **codec)
+    k, v = _outlier_inputs(wl, 11)
+    cache = K.make_gpu_cache(wl, seq + 8)
+    cache.prefill(0, k.cuda(), v.cuda())
+    oc = O.OracleCache(K.spec_of(wl), 2)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    torch.cuda.synchronize()
+    for n in range(2):
+        K.assert_state_equal(K.gpu_state(cache, 0, n), K.oracle_state(oc, n), "n=%d" % n)
+    assert cache.status() == 0
+
+
+@pytest.mark.parametrize("name,codec", NO_OUTLIER_CODECS[:4], ids=[c[0] for c in NO_OUTLIER_CODECS[:4]])
+def test_outlier_split_with_exact_ties(name, codec):
+    wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=2, num_kv_heads=2, seq_len=400,
+                 outliers_per_row=2, **codec)
+    k, v = _tie_inputs(wl, 9)
+    cache = K.make_gpu_cache(wl, 420)
+    cache.prefill(0, k.cuda(), v.cuda())
+    oc = O.OracleCache(K.spec_of(wl), 2)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    torch.cuda.synchronize()
+    for n in range(2):
+        K.assert_state_equal(K.gpu_state(cache, 0, n), K.oracle_state(oc, n), "n=%d" % n)
+    assert cache.status() == 0
+
+
 TC_CODECS = [
     ("k3v3g128", dict(k_bits=3, v_bits=3, k_group=128, v_group=128)),
     ("k4v4g64", dict(k_bits=4, v_bits=4, k_group=64, v_group=64)),
