@@ -332,6 +332,19 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
   float vsf[VGPR];  // 2^(6 - ev[q])
   uint32_t pw[VGPR];
   const bool one_head = NT == 1 && G == 1;  // warp-uniform
+  // One query head: value-outlier corrections p_t (x - z_t) of the lane's
+  // token go through a four-entry cache of (channel, sum) in registers, so
+  // that the few channels that hold most outliers are summed without shared
+  // memory atomics; an entry is added into ocr when it is evicted and at the
+  // end.
+  int occ[4];
+  float oca[4];
+  int ovic = 0;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    occ[k] = -1;
+    oca[k] = 0.0f;
+  }
 
   auto front = [&](int tj) -> bool {
     {
@@ -610,6 +623,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
   #pragma unroll
               for (int k = 0; k < 4; ++k) ocr[h * kHeadDim + lane + 32 * k] *= alh;
             }
+            if (one_head) {
+              const float al0 = __shfl_sync(kFull, al, 0);
+#pragma unroll
+              for (int k = 0; k < 4; ++k) oca[k] *= al0;
+            }
             __syncwarp();
           }
           m_run[nt] = mnew;
@@ -624,7 +642,38 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
       }
 
       // ---- value outliers: o_c += p_t (x - z_t), one row per lane ----------------
-      if (OUTL) {
+      if (OUTL && one_head) {
+        const int src = 4 * (lane & 7);  // head 0 lives in lanes with t4 = 0
+        const float p00 = __shfl_sync(kFull, p[0][0][0], src), p01 = __shfl_sync(kFull, p[0][0][1], src);
+        const float p10 = __shfl_sync(kFull, p[0][1][0], src), p11 = __shfl_sync(kFull, p[0][1][1], src);
+        const float pl = (lane & 16) ? ((lane & 8) ? p11 : p10) : ((lane & 8) ? p01 : p00);
+        if (t0 + lane < row_end) {
+          const uint16_t* vcol = reinterpret_cast<const uint16_t*>(ot + 4 * kRows * kout);
+          const __half* vval = reinterpret_cast<const __half*>(ot + 6 * kRows * kout);
+          for (int e = 0; e < kout; ++e) {
+            const int c = vcol[lane * kout + e] & (kHeadDim - 1);
+            const float d = __half2float(vval[lane * kout + e]) - __high2float(vm[lane * VGPR + c / VG]);
+            const float v = pl * d;
+            bool hit = false;
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              if (occ[k] == c) {
+                oca[k] += v;
+                hit = true;
+              }
+            if (!hit) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                if (k == ovic) {
+                  if (occ[k] >= 0) atomicAdd(&ocr[occ[k]], oca[k]);
+                  occ[k] = c;
+                  oca[k] = v;
+                }
+              ovic = (ovic + 1) & 3;
+            }
+          }
+        }
+      } else if (OUTL) {
   #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
   #pragma unroll
@@ -839,6 +888,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
     }
     middle(ti);
     back(ti);
+  }
+  if (OUTL && one_head) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (occ[k] >= 0) atomicAdd(&ocr[occ[k]], oca[k]);
   }
   if (failed && lane == 0) {
     raise_status(L.status, kStatusTimeout);

@@ -244,13 +244,12 @@ __device__ __forceinline__ void slow_chunk(uint32_t (&wa)[BITS / 4], XAt x_at, Z
 // 0.
 //
 // Selection works on packed fp16 magnitudes (sign bits cleared; for
-// non-negative halves the fp16 order is the order of |x|). Round r takes
-// M_r = max{|x| : |x| < M_(r-1)} over the row (lanes reduce by shuffles);
-// after k rounds the slots with |x| >= M_k are the outliers exactly when
-// there are k of them. Otherwise a magnitude repeats at the top of the row
-// (a tie), and the warp redoes the selection with unique keys
-// (|x| bits << 16) | (128 - channel): round r then takes the largest key
-// below the one round r-1 took.
+// non-negative halves the fp16 order is the order of |x|). A threshold t
+// (the k-th largest |x| of the row, see kth_magnitude) marks the slots with
+// |x| >= t; they are the outliers exactly when there are k of them.
+// Otherwise a magnitude repeats at the threshold (a tie), and the warp redoes
+// the selection with unique keys (|x| bits << 16) | (128 - channel): round r
+// takes the largest key below the one round r-1 took.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t hmax2_bits(uint32_t a, uint32_t b) {
   const __half2 r = __hmax2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
@@ -276,9 +275,42 @@ __device__ __forceinline__ uint32_t row_max2(const uint32_t (&v)[NP]) {
   return m;
 }
 
-// M_k of the row (k >= 1) from the magnitudes a of this lane's pairs.
+__device__ __forceinline__ uint32_t hmin2_bits(uint32_t a, uint32_t b) {
+  const __half2 r = __hmin2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+
+// The second largest magnitude of the row, counted with multiplicity (equal
+// to the largest when that occurs twice): per half a running (largest,
+// second) pair, then pairs merge across the halves and the NL lanes.
+template <int NP, int NL>
+__device__ __forceinline__ uint32_t row_second2(const uint32_t (&a)[NP]) {
+  uint32_t m1 = a[0], m2 = 0u;
+#pragma unroll
+  for (int p = 1; p < NP; ++p) {
+    m2 = hmax2_bits(m2, hmin2_bits(m1, a[p]));
+    m1 = hmax2_bits(m1, a[p]);
+  }
+  auto merge = [](uint32_t& x1, uint32_t& x2, uint32_t y1, uint32_t y2) {
+    x2 = hmax2_bits(hmin2_bits(x1, y1), hmax2_bits(x2, y2));
+    x1 = hmax2_bits(x1, y1);
+  };
+  merge(m1, m2, __byte_perm(m1, 0u, 0x1032u), __byte_perm(m2, 0u, 0x1032u));
+#pragma unroll
+  for (int off = 1; off < NL; off <<= 1) {
+    const uint32_t y1 = __shfl_xor_sync(kFull, m1, off), y2 = __shfl_xor_sync(kFull, m2, off);
+    merge(m1, m2, y1, y2);
+  }
+  return m2;
+}
+
+// The outlier threshold of the row from the magnitudes a of this lane's
+// pairs: k = 1 the largest, k = 2 the second largest with multiplicity,
+// k > 2 the k-th largest distinct magnitude M_k. The slots at or above it
+// are the outliers when they number k.
 template <int NP, int NL>
 __device__ __forceinline__ uint32_t kth_magnitude(const uint32_t (&a)[NP], int kout) {
+  if (kout == 2) return row_second2<NP, NL>(a);
   uint32_t m = row_max2<NP, NL>(a);
   for (int r = 1; r < kout; ++r) {
     uint32_t b[NP];
@@ -411,130 +443,158 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
   const int sw = q >> 2;
   const int lpg = T.group >> 4;  // lanes per group (groups of 16 .. 128 channels)
   const int per_row = kHeadDim / T.group;
-#pragma unroll 2
+#pragma unroll(OUTL ? 1 : 2)  // outlier selection makes the body long enough
   for (int it = 0; it < RPW / 4; ++it) {
     const int lr = warp * RPW + it * 4 + rr;
     const bool live = lr < nrows;
     const uint4* rowp = reinterpret_cast<const uint4*>(tile + (size_t)lr * (kHeadDim * 2));
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(rowp);
     const int c0 = 2 * q + sw, c1 = 2 * q + 1 - sw;  // chunk indices of raw0, raw1
-    uint4 raw0 = rowp[c0], raw1 = rowp[c1];
     // outliers: om0 / om1 bit e <- element e of chunk c0 / c1; mk[p] the
-    // mask of pair p (pairs 0-3 of raw0, 4-7 of raw1)
+    // mask of pair p (pairs 0-3 of raw0, 4-7 of raw1); first: entries of
+    // the row before this lane's
     uint32_t om0 = 0, om1 = 0, mk[8];
-    if (OUTL) {
-      const uint32_t wv[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
-      uint32_t a[8];
-#pragma unroll
-      for (int p = 0; p < 8; ++p) a[p] = wv[p] & 0x7FFF7FFFu;
-      const uint32_t mk_th = kth_magnitude<8, 8>(a, kout);
-#pragma unroll
-      for (int p = 0; p < 8; ++p) mk[p] = ge_mask(a[p], mk_th);
-      om0 = mask_bits<4>(*reinterpret_cast<const uint32_t(*)[4]>(&mk[0]));
-      om1 = mask_bits<4>(*reinterpret_cast<const uint32_t(*)[4]>(&mk[4]));
-      int total;
-      int first = row_scan<8>(__popc(om0) + __popc(om1), q, total);
-      if (__any_sync(kFull, total != kout)) {
-        // a repeated magnitude at the top of some row: unique keys
-        const uint16_t* hx0 = reinterpret_cast<const uint16_t*>(&raw0);
-        const uint16_t* hx1 = reinterpret_cast<const uint16_t*>(&raw1);
-        uint32_t key[16];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          key[e] = outlier_key(hx0[e], 8 * c0 + e);
-          key[8 + e] = outlier_key(hx1[e], 8 * c1 + e);
-        }
-        const uint32_t kw = kth_key<8, 16>(key, kout);
-        om0 = 0;
-        om1 = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          om0 |= (key[e] >= kw ? 1u : 0u) << e;
-          om1 |= (key[8 + e] >= kw ? 1u : 0u) << e;
-        }
-        expand_mask4(om0, *reinterpret_cast<uint32_t(*)[4]>(&mk[0]));
-        expand_mask4(om1, *reinterpret_cast<uint32_t(*)[4]>(&mk[4]));
-        first = row_scan<8>(__popc(om0) + __popc(om1), q, total);
-      }
-      if (live) {
-        const uint16_t* xs = reinterpret_cast<const uint16_t*>(rowp);
-        const uint32_t om16 = sw ? (om1 | (om0 << 8)) : (om0 | (om1 << 8));  // channel order
-        write_lane_csr(T, n, row0 + lr, kout, om16, 16 * q, first, xs);
-        if (q == 0) write_rowptr(T, n, row0 + lr, kout);
-      }
-      if (SYM) {
-        // an outlier slot reads +0: the absolute maximum of the rest stays,
-        // and the slot codes 0
-        raw0 = make_uint4(wv[0] & ~mk[0], wv[1] & ~mk[1], wv[2] & ~mk[2], wv[3] & ~mk[3]);
-        raw1 = make_uint4(wv[4] & ~mk[4], wv[5] & ~mk[5], wv[6] & ~mk[6], wv[7] & ~mk[7]);
-      }
-    }
-    const __half2* h0 = reinterpret_cast<const __half2*>(&raw0);
-    const __half2* h1 = reinterpret_cast<const __half2*>(&raw1);
-    float s, nz = 0.0f, rlo, rhi;
-    bool slow;
+    int first = 0;
     __half s16, z16;
-    if (SYM) {
-      __half2 m = __habs2(h0[0]);
-#pragma unroll
-      for (int j = 1; j < 4; ++j) m = __hmax2(m, __habs2(h0[j]));
-#pragma unroll
-      for (int j = 0; j < 4; ++j) m = __hmax2(m, __habs2(h1[j]));
-      m = __hmax2(m, __lowhigh2highlow(m));
-      for (int off = 1; off < lpg; off <<= 1) {
-        const uint32_t o = __shfl_xor_sync(kFull, *reinterpret_cast<uint32_t*>(&m), off);
-        m = __hmax2(m, *reinterpret_cast<const __half2*>(&o));
-      }
-      const float am = __low2float(m);  // |x| >= 0, canonical +0
-      s16 = __float2half_rn(div_levels<kLev>(am));
-      z16 = __ushort_as_half(0);
-    } else {
-      __half2 vn[8], vx[8];
-#pragma unroll
-      for (int p = 0; p < 8; ++p) {
-        const __half2 h = p < 4 ? h0[p] : h1[p - 4];
-        if (OUTL) {
-          // outlier slots read +inf for the minimum and -inf for the maximum
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(&h);
-          const uint32_t wn = (w & ~mk[p]) | (0x7C007C00u & mk[p]);
-          const uint32_t wx = (w & ~mk[p]) | (0xFC00FC00u & mk[p]);
-          vn[p] = *reinterpret_cast<const __half2*>(&wn);
-          vx[p] = *reinterpret_cast<const __half2*>(&wx);
-        } else {
-          vn[p] = h;
-          vx[p] = h;
-        }
-      }
-      __half2 mn = __hmin2(vn[0], vn[1]), mx = __hmax2(vx[0], vx[1]);
-      mn = __hmin2(mn, __hmin2(vn[2], vn[3]));
-      mx = __hmax2(mx, __hmax2(vx[2], vx[3]));
-      mn = __hmin2(mn, __hmin2(__hmin2(vn[4], vn[5]), __hmin2(vn[6], vn[7])));
-      mx = __hmax2(mx, __hmax2(__hmax2(vx[4], vx[5]), __hmax2(vx[6], vx[7])));
-      const __half2 nmx = __hneg2(mx);
-      __half2 pr = __hmin2(__lows2half2(mn, nmx), __highs2half2(mn, nmx));  // (min, -max)
-      for (int off = 1; off < lpg; off <<= 1) {
-        const uint32_t o = __shfl_xor_sync(kFull, *reinterpret_cast<uint32_t*>(&pr), off);
-        pr = __hmin2(pr, *reinterpret_cast<const __half2*>(&o));
-      }
-      // zero extremes are taken as +0
-      const float mnv = __fadd_rn(__low2float(pr), 0.0f);
-      const float mxv = __fadd_rn(-__high2float(pr), 0.0f);
-      s16 = __float2half_rn(div_levels<kLev>(__fsub_rn(mxv, mnv)));
-      z16 = __float2half_rn(mnv);
-      nz = -mnv;
+    uint32_t wa0[PB / 4], wa1[PB / 4];
+    // Pass 0 selects by threshold; a tie in any row of the warp (found
+    // only after the codes, so that the count's shuffles overlap them)
+    // sends the warp through pass 1 with unique keys.
+    for (int pass = 0;; ++pass) {
+      uint4 raw0 = rowp[c0], raw1 = rowp[c1];
+      int total = kout;
       if (OUTL) {
-        // an outlier slot codes the zero point: d = 0, code 0
-        const uint32_t z2 = (uint32_t)__half_as_ushort(z16) * 0x10001u;
-        uint32_t* r0 = reinterpret_cast<uint32_t*>(&raw0);
-        uint32_t* r1 = reinterpret_cast<uint32_t*>(&raw1);
+        const uint32_t wv[8] = {raw0.x, raw0.y, raw0.z, raw0.w, raw1.x, raw1.y, raw1.z, raw1.w};
+        if (pass == 0) {
+          uint32_t a[8];
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-          r0[p] = (r0[p] & ~mk[p]) | (z2 & mk[p]);
-          r1[p] = (r1[p] & ~mk[4 + p]) | (z2 & mk[4 + p]);
+          for (int p = 0; p < 8; ++p) a[p] = wv[p] & 0x7FFF7FFFu;
+          const uint32_t th = kth_magnitude<8, 8>(a, kout);
+#pragma unroll
+          for (int p = 0; p < 8; ++p) mk[p] = ge_mask(a[p], th);
+          om0 = mask_bits<4>(*reinterpret_cast<const uint32_t(*)[4]>(&mk[0]));
+          om1 = mask_bits<4>(*reinterpret_cast<const uint32_t(*)[4]>(&mk[4]));
+        } else {
+          const uint16_t* hx0 = reinterpret_cast<const uint16_t*>(&raw0);
+          const uint16_t* hx1 = reinterpret_cast<const uint16_t*>(&raw1);
+          uint32_t key[16];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            key[e] = outlier_key(hx0[e], 8 * c0 + e);
+            key[8 + e] = outlier_key(hx1[e], 8 * c1 + e);
+          }
+          const uint32_t kw = kth_key<8, 16>(key, kout);
+          om0 = 0;
+          om1 = 0;
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            om0 |= (key[e] >= kw ? 1u : 0u) << e;
+            om1 |= (key[8 + e] >= kw ? 1u : 0u) << e;
+          }
+          expand_mask4(om0, *reinterpret_cast<uint32_t(*)[4]>(&mk[0]));
+          expand_mask4(om1, *reinterpret_cast<uint32_t(*)[4]>(&mk[4]));
+        }
+        first = row_scan<8>(__popc(om0) + __popc(om1), q, total);
+        if (SYM) {
+          // an outlier slot reads +0: the absolute maximum of the rest
+          // stays, and the slot codes 0
+          raw0 = make_uint4(wv[0] & ~mk[0], wv[1] & ~mk[1], wv[2] & ~mk[2], wv[3] & ~mk[3]);
+          raw1 = make_uint4(wv[4] & ~mk[4], wv[5] & ~mk[5], wv[6] & ~mk[6], wv[7] & ~mk[7]);
         }
       }
+      const __half2* h0 = reinterpret_cast<const __half2*>(&raw0);
+      const __half2* h1 = reinterpret_cast<const __half2*>(&raw1);
+      float nz = 0.0f, rlo, rhi;
+      bool slow;
+      if (SYM) {
+        __half2 m = __habs2(h0[0]);
+#pragma unroll
+        for (int j = 1; j < 4; ++j) m = __hmax2(m, __habs2(h0[j]));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m = __hmax2(m, __habs2(h1[j]));
+        m = __hmax2(m, __lowhigh2highlow(m));
+        for (int off = 1; off < lpg; off <<= 1) {
+          const uint32_t o = __shfl_xor_sync(kFull, *reinterpret_cast<uint32_t*>(&m), off);
+          m = __hmax2(m, *reinterpret_cast<const __half2*>(&o));
+        }
+        const float am = __low2float(m);  // |x| >= 0, canonical +0
+        s16 = __float2half_rn(div_levels<kLev>(am));
+        z16 = __ushort_as_half(0);
+      } else {
+        __half2 vn[8], vx[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+          const __half2 h = p < 4 ? h0[p] : h1[p - 4];
+          if (OUTL) {
+            // outlier slots read +inf for the minimum and -inf for the maximum
+            const uint32_t w = *reinterpret_cast<const uint32_t*>(&h);
+            const uint32_t wn = (w & ~mk[p]) | (0x7C007C00u & mk[p]);
+            const uint32_t wx = (w & ~mk[p]) | (0xFC00FC00u & mk[p]);
+            vn[p] = *reinterpret_cast<const __half2*>(&wn);
+            vx[p] = *reinterpret_cast<const __half2*>(&wx);
+          } else {
+            vn[p] = h;
+            vx[p] = h;
+          }
+        }
+        __half2 mn = __hmin2(vn[0], vn[1]), mx = __hmax2(vx[0], vx[1]);
+        mn = __hmin2(mn, __hmin2(vn[2], vn[3]));
+        mx = __hmax2(mx, __hmax2(vx[2], vx[3]));
+        mn = __hmin2(mn, __hmin2(__hmin2(vn[4], vn[5]), __hmin2(vn[6], vn[7])));
+        mx = __hmax2(mx, __hmax2(__hmax2(vx[4], vx[5]), __hmax2(vx[6], vx[7])));
+        const __half2 nmx = __hneg2(mx);
+        __half2 pr = __hmin2(__lows2half2(mn, nmx), __highs2half2(mn, nmx));  // (min, -max)
+        for (int off = 1; off < lpg; off <<= 1) {
+          const uint32_t o = __shfl_xor_sync(kFull, *reinterpret_cast<uint32_t*>(&pr), off);
+          pr = __hmin2(pr, *reinterpret_cast<const __half2*>(&o));
+        }
+        // zero extremes are taken as +0
+        const float mnv = __fadd_rn(__low2float(pr), 0.0f);
+        const float mxv = __fadd_rn(-__high2float(pr), 0.0f);
+        s16 = __float2half_rn(div_levels<kLev>(__fsub_rn(mxv, mnv)));
+        z16 = __float2half_rn(mnv);
+        nz = -mnv;
+        if (OUTL) {
+          // an outlier slot codes the zero point: d = 0, code 0
+          const uint32_t z2 = (uint32_t)__half_as_ushort(z16) * 0x10001u;
+          uint32_t* r0 = reinterpret_cast<uint32_t*>(&raw0);
+          uint32_t* r1 = reinterpret_cast<uint32_t*>(&raw1);
+#pragma unroll
+          for (int p = 0; p < 4; ++p) {
+            r0[p] = (r0[p] & ~mk[p]) | (z2 & mk[p]);
+            r1[p] = (r1[p] & ~mk[4 + p]) | (z2 & mk[4 + p]);
+          }
+        }
+      }
+      const float s = __half2float(s16);
+      scale_bracket(s, rlo, rhi, slow);
+      uint32_t wb0[PB / 4], wb1[PB / 4];
+      const Bcast<float> NZ{nz}, RL{rlo};
+      auto xat0 = [&](int i) { return xs[8 * c0 + i]; };
+      auto xat1 = [&](int i) { return xs[8 * c1 + i]; };
+      auto zat = [&](int) { return nz; };
+      auto sat = [&](int) { return s; };
+      auto rat = [&](int) { return rlo; };
+      if (!__any_sync(kFull, slow)) {
+        chunk_codes<PB, SYM>(raw0, NZ, RL, Bcast<float>{rhi}, wa0, wb0);
+        chunk_codes<PB, SYM>(raw1, NZ, RL, Bcast<float>{rhi}, wa1, wb1);
+        uint32_t diff = 0;
+#pragma unroll
+        for (int j = 0; j < PB / 4; ++j) diff |= (wa0[j] ^ wb0[j]) | (wa1[j] ^ wb1[j]);
+        if (__any_sync(kFull, diff != 0)) {
+          settle_chunk<PB, SYM>(wa0, wb0, xat0, zat, sat, rat);
+          settle_chunk<PB, SYM>(wa1, wb1, xat1, zat, sat, rat);
+        }
+      } else {
+        slow_chunk<PB, SYM, kLev>(wa0, xat0, zat, sat);
+        slow_chunk<PB, SYM, kLev>(wa1, xat1, zat, sat);
+        if (OUTL) {  // the IEEE path coded the outliers' own values
+          for (uint32_t m = om0; m; m &= m - 1) clear_field<PB>(wa0, __ffs(m) - 1);
+          for (uint32_t m = om1; m; m &= m - 1) clear_field<PB>(wa1, __ffs(m) - 1);
+        }
+      }
+      if (!OUTL || pass > 0 || !__any_sync(kFull, total != kout)) break;
     }
-    s = __half2float(s16);
-    scale_bracket(s, rlo, rhi, slow);
     if (live && (q & (lpg - 1)) == 0) {
       unsigned char* mb = T.meta + (int64_t)n * T.meta_sstride;
       const int64_t at = (int64_t)(row0 + lr) * per_row + q / lpg;
@@ -543,31 +603,10 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
       else
         reinterpret_cast<__half2*>(mb)[at] = __halves2half2(s16, z16);
     }
-    uint32_t wa0[PB / 4], wb0[PB / 4], wa1[PB / 4], wb1[PB / 4];
-    const uint16_t* xs = reinterpret_cast<const uint16_t*>(rowp);
-    const Bcast<float> NZ{nz}, RL{rlo};
-    auto xat0 = [&](int i) { return xs[8 * c0 + i]; };
-    auto xat1 = [&](int i) { return xs[8 * c1 + i]; };
-    auto zat = [&](int) { return nz; };
-    auto sat = [&](int) { return s; };
-    auto rat = [&](int) { return rlo; };
-    if (!__any_sync(kFull, slow)) {
-      chunk_codes<PB, SYM>(raw0, NZ, RL, Bcast<float>{rhi}, wa0, wb0);
-      chunk_codes<PB, SYM>(raw1, NZ, RL, Bcast<float>{rhi}, wa1, wb1);
-      uint32_t diff = 0;
-#pragma unroll
-      for (int j = 0; j < PB / 4; ++j) diff |= (wa0[j] ^ wb0[j]) | (wa1[j] ^ wb1[j]);
-      if (__any_sync(kFull, diff != 0)) {
-        settle_chunk<PB, SYM>(wa0, wb0, xat0, zat, sat, rat);
-        settle_chunk<PB, SYM>(wa1, wb1, xat1, zat, sat, rat);
-      }
-    } else {
-      slow_chunk<PB, SYM, kLev>(wa0, xat0, zat, sat);
-      slow_chunk<PB, SYM, kLev>(wa1, xat1, zat, sat);
-      if (OUTL) {  // the IEEE path coded the outliers' own values
-        for (uint32_t m = om0; m; m &= m - 1) clear_field<PB>(wa0, __ffs(m) - 1);
-        for (uint32_t m = om1; m; m &= m - 1) clear_field<PB>(wa1, __ffs(m) - 1);
-      }
+    if (OUTL && live) {
+      const uint32_t om16 = sw ? (om1 | (om0 << 8)) : (om0 | (om1 << 8));  // channel order
+      write_lane_csr(T, n, row0 + lr, kout, om16, 16 * q, first, xs);
+      if (q == 0) write_rowptr(T, n, row0 + lr, kout);
     }
     if (BITS == 3) {
       // ten codes per word: through this warp's row buffer (one byte per code)
@@ -608,7 +647,7 @@ struct KeyScratch {
 template <int BITS, int TB, bool OUTL>
 __device__ __forceinline__ bool key_block(const unsigned char* tile, const TensorDev& K, int n,
                                           int blk, bool ok, KeyScratch& ks, int warp, int lane,
-                                          unsigned char* rowbuf, int kout, uint8_t* ombuf) {
+                                          unsigned char* rowbuf, int kout, uint16_t* ombuf) {
   constexpr int kLev = (1 << BITS) - 1;
   constexpr int kRW = TB / kWarps;  // rows of this warp
   constexpr int kIt = kRW / 2;      // rows per lane
@@ -619,62 +658,65 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
   const __half2 pinf = __half2half2(__ushort_as_half(0x7C00));
   const __half2 ninf = __half2half2(__ushort_as_half(0xFC00));
   __half2 mn[4], mx[4];
+  // Pass 1: per-channel minima and maxima of the block. With outliers each
+  // token row (sixteen lanes hold it) first selects its outliers, which the
+  // statistics leave out; ombuf keeps the lane's bits and its first CSR
+  // position for the code pass. A tie in any row of the warp (a repeated
+  // magnitude at the threshold) repeats the pass with unique keys.
+  for (int pass = 0; pass < (OUTL ? 2 : 1); ++pass) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    mn[j] = pinf;
-    mx[j] = ninf;
-  }
-#pragma unroll 4
-  for (int i = 0; i < kIt; ++i) {
-    const int row = warp * kRW + 2 * i + p;
-    const uint4 raw = t4[row * 16 + o];
-    const __half2* h = reinterpret_cast<const __half2*>(&raw);
-    if (OUTL) {
-      // outliers of token row `row` (sixteen lanes hold it), left out of the
-      // per-channel statistics; the lane's bits are kept for the code pass
-      const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-      uint32_t a[4], mk[4];
+    for (int j = 0; j < 4; ++j) {
+      mn[j] = pinf;
+      mx[j] = ninf;
+    }
+    bool tie = false;
+#pragma unroll(OUTL ? 2 : 4)
+    for (int i = 0; i < kIt; ++i) {
+      const int row = warp * kRW + 2 * i + p;
+      const uint4 raw = t4[row * 16 + o];
+      const __half2* h = reinterpret_cast<const __half2*>(&raw);
+      if (OUTL) {
+        const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t mk[4], om;
+        if (pass == 0) {
+          uint32_t a[4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) a[j] = wv[j] & 0x7FFF7FFFu;
-      const uint32_t th = kth_magnitude<4, 16>(a, kout);
+          for (int j = 0; j < 4; ++j) a[j] = wv[j] & 0x7FFF7FFFu;
+          const uint32_t th = kth_magnitude<4, 16>(a, kout);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) mk[j] = ge_mask(a[j], th);
-      uint32_t om = mask_bits<4>(mk);
-      int total;
-      int first = row_scan<16>(__popc(om), o, total);
-      if (__any_sync(kFull, total != kout)) {
-        // a repeated magnitude at the top of some row: unique keys
-        const uint16_t* hx = reinterpret_cast<const uint16_t*>(&raw);
-        uint32_t key[8];
+          for (int j = 0; j < 4; ++j) mk[j] = ge_mask(a[j], th);
+          om = mask_bits<4>(mk);
+        } else {
+          const uint16_t* hx = reinterpret_cast<const uint16_t*>(&raw);
+          uint32_t key[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) key[e] = outlier_key(hx[e], 8 * o + e);
-        const uint32_t kw = kth_key<16, 8>(key, kout);
-        om = 0;
+          for (int e = 0; e < 8; ++e) key[e] = outlier_key(hx[e], 8 * o + e);
+          const uint32_t kw = kth_key<16, 8>(key, kout);
+          om = 0;
 #pragma unroll
-        for (int e = 0; e < 8; ++e) om |= (key[e] >= kw ? 1u : 0u) << e;
-        expand_mask4(om, mk);
-        first = row_scan<16>(__popc(om), o, total);
-      }
-      if (ok) {
-        write_lane_csr(K, n, blk * TB + row, kout, om, 8 * o, first,
-                       reinterpret_cast<const uint16_t*>(tile + (size_t)row * kHeadDim * 2));
-        if (o == 0) write_rowptr(K, n, blk * TB + row, kout);
-      }
-      ombuf[i * 32 + lane] = (uint8_t)om;
+          for (int e = 0; e < 8; ++e) om |= (key[e] >= kw ? 1u : 0u) << e;
+          expand_mask4(om, mk);
+        }
+        int total;
+        const int first = row_scan<16>(__popc(om), o, total);
+        tie |= total != kout;
+        ombuf[i * 32 + lane] = (uint16_t)(om | ((uint32_t)first << 8));
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const uint32_t wn = (wv[j] & ~mk[j]) | (0x7C007C00u & mk[j]);  // +inf
-        const uint32_t wx = (wv[j] & ~mk[j]) | (0xFC00FC00u & mk[j]);  // -inf
-        mn[j] = __hmin2(mn[j], *reinterpret_cast<const __half2*>(&wn));
-        mx[j] = __hmax2(mx[j], *reinterpret_cast<const __half2*>(&wx));
-      }
-    } else {
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t wn = (wv[j] & ~mk[j]) | (0x7C007C00u & mk[j]);  // +inf
+          const uint32_t wx = (wv[j] & ~mk[j]) | (0xFC00FC00u & mk[j]);  // -inf
+          mn[j] = __hmin2(mn[j], *reinterpret_cast<const __half2*>(&wn));
+          mx[j] = __hmax2(mx[j], *reinterpret_cast<const __half2*>(&wx));
+        }
+      } else {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        mn[j] = __hmin2(mn[j], h[j]);
-        mx[j] = __hmax2(mx[j], h[j]);
+        for (int j = 0; j < 4; ++j) {
+          mn[j] = __hmin2(mn[j], h[j]);
+          mx[j] = __hmax2(mx[j], h[j]);
+        }
       }
     }
+    if (!OUTL || !__any_sync(kFull, tie)) break;
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
@@ -746,8 +788,11 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
     uint4 raw = t4[row * 16 + o];
     auto xat = [&](int e) { return xs[row * kHeadDim + 8 * o + e]; };
     uint32_t wa[PB / 4], wb[PB / 4];
-    const uint32_t om = OUTL ? ombuf[i * 32 + lane] : 0u;
+    const uint32_t oe = OUTL ? ombuf[i * 32 + lane] : 0u;
+    const uint32_t om = oe & 0xFFu;
     if (OUTL) {
+      write_lane_csr(K, n, blk * TB + row, kout, om, 8 * o, (int)(oe >> 8), xs + row * kHeadDim);
+      if (o == 0) write_rowptr(K, n, blk * TB + row, kout);
       // an outlier slot codes its channel's zero point (code 0 in both
       // brackets): its own value may lie outside the range, and a field out
       // of range would carry into its neighbours when the fields are summed
@@ -809,7 +854,7 @@ struct Geo {
   static constexpr size_t kScratch = kPerChannel ? sizeof(KeyScratch) : 0;
   static constexpr size_t kRowBuf = (KB == 3 || VB == 3) ? 4 * kHeadDim : 0;  // per warp, 3-bit repacking
   // per warp, the outlier masks of its key-block rows between the two passes
-  static constexpr size_t kOmBuf = (kPerChannel && OUTL) ? (size_t)TB / 8 * 32 : 0;
+  static constexpr size_t kOmBuf = (kPerChannel && OUTL) ? (size_t)TB / 8 * 32 * 2 : 0;
   static constexpr size_t kCtl = 64;  // counters and barriers
   static constexpr size_t kBytes =
       (size_t)kStages * kStageBytes + kScratch + kWarps * (kRowBuf + kOmBuf) + kCtl;
@@ -823,7 +868,8 @@ __global__ void __launch_bounds__(kThreads, 4) prefill_fast_kernel(Args a) {
   extern __shared__ __align__(128) unsigned char smem[];
   KeyScratch& ks = *reinterpret_cast<KeyScratch*>(smem + S * G::kStageBytes);
   unsigned char* rowbuf = smem + S * G::kStageBytes + G::kScratch + (size_t)(threadIdx.x >> 5) * G::kRowBuf;
-  uint8_t* ombuf = smem + S * G::kStageBytes + G::kScratch + kWarps * G::kRowBuf + (size_t)(threadIdx.x >> 5) * G::kOmBuf;
+  uint16_t* ombuf = reinterpret_cast<uint16_t*>(smem + S * G::kStageBytes + G::kScratch + kWarps * G::kRowBuf +
+                                                (size_t)(threadIdx.x >> 5) * G::kOmBuf);
   unsigned char* ctl = smem + S * G::kStageBytes + G::kScratch + kWarps * (G::kRowBuf + G::kOmBuf);
   int* cnt = reinterpret_cast<int*>(ctl);           // [S] warps done with a stage
   int* issued = reinterpret_cast<int*>(ctl + 16);   // [S] copies issued into a stage
