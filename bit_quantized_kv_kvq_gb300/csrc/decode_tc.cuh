@@ -333,13 +333,14 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
   uint32_t pw[VGPR];
   const bool one_head = NT == 1 && G == 1;  // warp-uniform
   // One query head: value-outlier corrections p_t (x - z_t) of the lane's
-  // token go through a four-entry cache of (channel, sum) in registers, so
-  // that the few channels that hold most outliers are summed without shared
-  // memory atomics; an entry is added into ocr when it is evicted and at the
-  // end.
+  // tokens are summed in registers for the first four channels the lane
+  // meets (outliers gather in a few channels, which then stay in registers
+  // for the whole split) and added into ocr at the end; other channels go
+  // to ocr by shared-memory atomics. Evicting entries would send the
+  // frequent channels back through the atomics, which conflict.
   int occ[4];
   float oca[4];
-  int ovic = 0;
+  int ovic = 0;  // entries in use
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     occ[k] = -1;
@@ -662,14 +663,17 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
                 hit = true;
               }
             if (!hit) {
+              if (ovic < 4) {  // a free entry: the channel keeps it
 #pragma unroll
-              for (int k = 0; k < 4; ++k)
-                if (k == ovic) {
-                  if (occ[k] >= 0) atomicAdd(&ocr[occ[k]], oca[k]);
-                  occ[k] = c;
-                  oca[k] = v;
-                }
-              ovic = (ovic + 1) & 3;
+                for (int k = 0; k < 4; ++k)
+                  if (k == ovic) {
+                    occ[k] = c;
+                    oca[k] = v;
+                  }
+                ++ovic;
+              } else {
+                atomicAdd(&ocr[c], v);
+              }
             }
           }
         }
