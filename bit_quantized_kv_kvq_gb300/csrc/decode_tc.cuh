@@ -543,7 +543,25 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
       }
 
       // ---- key outliers: score += q_c (x - z_c), one row per lane ---------------
-      if (OUTL) {
+      if (OUTL && one_head) {
+        if (!rt) {
+          // one head: the lane's row correction reaches the score owners by
+          // shuffles
+          const __half* kval = reinterpret_cast<const __half*>(ot + 2 * kRows * kout);
+          const int ke = (t0 + lane < row_end) ? kout : 0;
+          const uint16_t* kcol = reinterpret_cast<const uint16_t*>(ot);
+          float corr = 0.0f;
+          for (int e = 0; e < ke; ++e) {
+            const int c = kcol[lane * kout + e] & (kHeadDim - 1);
+            const float d = __half2float(kval[lane * kout + e]) - __high2float(km[c]);
+            corr = fmaf(qf[c], d, corr);
+          }
+  #pragma unroll
+          for (int mt = 0; mt < 2; ++mt)
+  #pragma unroll
+            for (int r = 0; r < 2; ++r) sc[0][mt][r] += __shfl_sync(kFull, corr, 16 * mt + g + 8 * r);
+        }
+      } else if (OUTL) {
         if (!rt) {
           const __half* kval = reinterpret_cast<const __half*>(ot + 2 * kRows * kout);
           const int ke = (t0 + lane < row_end) ? kout : 0;
