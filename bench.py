@@ -451,6 +451,8 @@ def profile_case(args, wl):
 
     if args.batch:
         wl = dataclasses.replace(wl, batch=args.batch)
+    if args.seq:
+        wl = dataclasses.replace(wl, seq_len=args.seq)
     device = torch.device("cuda", 0)
     S = wl.seq_len
     cache = kvq.QuantizedKVCache(1, wl.batch, wl.num_kv_heads, wl.head_dim, S + 1, wl.k_bits,
@@ -466,7 +468,8 @@ def profile_case(args, wl):
     torch.cuda.synchronize(device)
     if cache.status() != 0:
         raise RuntimeError("device status word %#x" % cache.status())
-    print(json.dumps({"profile_case": wl.name, "batch": wl.batch, "reps": args.reps}), flush=True)
+    print(json.dumps({"profile_case": wl.name, "batch": wl.batch, "seq_len": wl.seq_len, "reps": args.reps}),
+          flush=True)
 
 
 def main(argv=None):
@@ -482,6 +485,7 @@ def main(argv=None):
                     help="untimed prefill/append/decode repetitions for a profiler")
     ap.add_argument("--batch", type=int, default=0, help="batch of --profile-case (0: workload's)")
     ap.add_argument("--reps", type=int, default=2, help="repetitions of --profile-case")
+    ap.add_argument("--seq", type=int, default=0, help="context length of --profile-case (0: workload's)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
