@@ -551,6 +551,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
           const int ke = (t0 + lane < row_end) ? kout : 0;
           const uint16_t* kcol = reinterpret_cast<const uint16_t*>(ot);
           float corr = 0.0f;
+#pragma unroll 2
           for (int e = 0; e < ke; ++e) {
             const int c = kcol[lane * kout + e] & (kHeadDim - 1);
             const float d = __half2float(kval[lane * kout + e]) - __high2float(km[c]);
@@ -669,10 +670,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
         if (t0 + lane < row_end) {
           const uint16_t* vcol = reinterpret_cast<const uint16_t*>(ot + 4 * kRows * kout);
           const __half* vval = reinterpret_cast<const __half*>(ot + 6 * kRows * kout);
-          for (int e = 0; e < kout; ++e) {
-            const int c = vcol[lane * kout + e] & (kHeadDim - 1);
-            const float d = __half2float(vval[lane * kout + e]) - __high2float(vm[lane * VGPR + c / VG]);
-            const float v = pl * d;
+          // zero points of the token's value groups (at most two: VG >= 64)
+          float zq[VGPR];
+#pragma unroll
+          for (int q = 0; q < VGPR; ++q) zq[q] = __high2float(vm[lane * VGPR + q]);
+          auto upd = [&](int c, float v) {
             bool hit = false;
 #pragma unroll
             for (int k = 0; k < 4; ++k)
@@ -693,6 +695,17 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
                 atomicAdd(&ocr[c], v);
               }
             }
+          };
+          // two entries per step: their loads overlap
+          for (int e = 0; e < kout; e += 2) {
+            const bool two = e + 1 < kout;
+            const int i0 = lane * kout + e, i1 = two ? i0 + 1 : i0;
+            const int c0 = vcol[i0] & (kHeadDim - 1), c1 = vcol[i1] & (kHeadDim - 1);
+            const float x0 = __half2float(vval[i0]), x1 = __half2float(vval[i1]);
+            const float z0 = VGPR == 1 ? zq[0] : (c0 < VG ? zq[0] : zq[VGPR - 1]);
+            const float z1 = VGPR == 1 ? zq[0] : (c1 < VG ? zq[0] : zq[VGPR - 1]);
+            upd(c0, pl * (x0 - z0));
+            if (two) upd(c1, pl * (x1 - z1));
           }
         }
       } else if (OUTL) {
