@@ -352,6 +352,18 @@ def test_tensor_core_decode_grid(name, codec, gqa, outliers):
     _run_case(wl, appends=2, check_every=1)
 
 
+@pytest.mark.parametrize("kout", [1, 3, 8])
+@pytest.mark.parametrize("gqa", [1, 4])
+@pytest.mark.parametrize("vg", [64, 128])
+def test_tensor_core_decode_outlier_counts(kout, gqa, vg):
+    """Outlier counts other than two: an unpaired last entry (1, 3) and more
+    channels per lane than the value-correction register cache holds (8),
+    with one query head (register cache) and a group (shared atomics)."""
+    wl = replace(W.DENSE_SPARSE_128K, batch=1, num_kv_heads=2, num_q_heads=2 * gqa, seq_len=333,
+                 outliers_per_row=kout, v_group=vg)
+    _run_case(wl, appends=2, check_every=1)
+
+
 def test_tensor_core_decode_wide_value_scales():
     """Value groups whose scales span many powers of two (the fp16 operand
     keeps its precision through the running exponent)."""
