@@ -1,4 +1,6 @@
-// Prefill quantize for codecs without outliers (3-, 4- or 8-bit codes).
+// Prefill quantize (3-, 4- or 8-bit codes; per-token rows and per-channel key
+// blocks of 64 or 128 tokens), with or without the dense-and-sparse outlier
+// split (template parameter OUTL).
 //
 // One launch quantizes a whole prompt of one layer. CTAs of four warps are
 // persistent and take work items in a fixed order: a per-channel key block
