@@ -366,6 +366,38 @@ __device__ __forceinline__ uint32_t kth_key(const uint32_t (&key)[NE], int kout)
   return thr;
 }
 
+// The tie path, kept out of line (it runs for a few rows in a thousand): the
+// outlier bits of this lane's chunks by unique keys. Sixteen channels
+// (chunks c0, c1, eight lanes a row): returns bits of c0 | bits of c1 << 8.
+static __device__ __noinline__ uint32_t exact_bits16(uint4 raw0, uint4 raw1, int c0, int c1, int kout) {
+  const uint16_t* hx0 = reinterpret_cast<const uint16_t*>(&raw0);
+  const uint16_t* hx1 = reinterpret_cast<const uint16_t*>(&raw1);
+  uint32_t key[16];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    key[e] = outlier_key(hx0[e], 8 * c0 + e);
+    key[8 + e] = outlier_key(hx1[e], 8 * c1 + e);
+  }
+  const uint32_t kw = kth_key<8, 16>(key, kout);
+  uint32_t om = 0;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) om |= (key[e] >= kw ? 1u : 0u) << e;
+  return om;
+}
+
+// Eight channels (chunk o, sixteen lanes a row).
+static __device__ __noinline__ uint32_t exact_bits8(uint4 raw, int o, int kout) {
+  const uint16_t* hx = reinterpret_cast<const uint16_t*>(&raw);
+  uint32_t key[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) key[e] = outlier_key(hx[e], 8 * o + e);
+  const uint32_t kw = kth_key<16, 8>(key, kout);
+  uint32_t om = 0;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) om |= (key[e] >= kw ? 1u : 0u) << e;
+  return om;
+}
+
 // CSR entries of this lane's outliers (om: bit i <- channel ch0 + i, in
 // channel order) at positions first, first + 1, ... of the row; xs holds the
 // row's fp16 values.
@@ -477,22 +509,9 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
           om0 = mask_bits<4>(*reinterpret_cast<const uint32_t(*)[4]>(&mk[0]));
           om1 = mask_bits<4>(*reinterpret_cast<const uint32_t(*)[4]>(&mk[4]));
         } else {
-          const uint16_t* hx0 = reinterpret_cast<const uint16_t*>(&raw0);
-          const uint16_t* hx1 = reinterpret_cast<const uint16_t*>(&raw1);
-          uint32_t key[16];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            key[e] = outlier_key(hx0[e], 8 * c0 + e);
-            key[8 + e] = outlier_key(hx1[e], 8 * c1 + e);
-          }
-          const uint32_t kw = kth_key<8, 16>(key, kout);
-          om0 = 0;
-          om1 = 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            om0 |= (key[e] >= kw ? 1u : 0u) << e;
-            om1 |= (key[8 + e] >= kw ? 1u : 0u) << e;
-          }
+          const uint32_t ob = exact_bits16(raw0, raw1, c0, c1, kout);
+          om0 = ob & 0xFFu;
+          om1 = ob >> 8;
           expand_mask4(om0, *reinterpret_cast<uint32_t(*)[4]>(&mk[0]));
           expand_mask4(om1, *reinterpret_cast<uint32_t(*)[4]>(&mk[4]));
         }
@@ -689,14 +708,7 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
           for (int j = 0; j < 4; ++j) mk[j] = ge_mask(a[j], th);
           om = mask_bits<4>(mk);
         } else {
-          const uint16_t* hx = reinterpret_cast<const uint16_t*>(&raw);
-          uint32_t key[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) key[e] = outlier_key(hx[e], 8 * o + e);
-          const uint32_t kw = kth_key<16, 8>(key, kout);
-          om = 0;
-#pragma unroll
-          for (int e = 0; e < 8; ++e) om |= (key[e] >= kw ? 1u : 0u) << e;
+          om = exact_bits8(raw, o, kout);
           expand_mask4(om, mk);
         }
         int total;
