@@ -190,8 +190,10 @@ struct Cfg {
 // 2^e as a float for -126 <= e <= 127.
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
+// Outlier variants hold about 68 KB of shared memory, so three CTAs per SM
+// at most: they get the register budget of three.
 template <int KB, int VB, int VG, int NT, bool OUTL>
-__global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
+__global__ void __launch_bounds__(kThreads, (NT == 1 && !OUTL) ? 4 : 3)
     decode_tc_kernel(LayerDev L, DecodeArgs a) {
   using C = Cfg<KB, VB, VG, NT, OUTL>;
   constexpr int S = C::kStages;
