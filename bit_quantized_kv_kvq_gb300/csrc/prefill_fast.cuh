@@ -36,8 +36,6 @@ namespace kvq {
 namespace pfx {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kWarps = 4;
-constexpr int kThreads = 32 * kWarps;
 constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23: x + kMagic holds rne(x) in its low bits
 constexpr uint32_t kMagicBits = 0x4B400000u;
 constexpr float kMinNormal16 = 0x1p-14f;
@@ -57,7 +55,8 @@ __device__ __forceinline__ uint32_t bfi(uint32_t field, uint32_t base, uint32_t 
   return r;
 }
 
-// Barrier of the four warps of the CTA that also ANDs a predicate over them.
+// Barrier of the NTH threads of the CTA that also ANDs a predicate over them.
+template <int NTH>
 __device__ __forceinline__ bool key_barrier_and(bool v) {
   uint32_t r;
   asm volatile(
@@ -66,7 +65,7 @@ __device__ __forceinline__ bool key_barrier_and(bool v) {
       "bar.red.and.pred p, %2, %3, q;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(r)
-      : "r"((uint32_t)v), "n"(kKeyBarrier), "n"(kThreads)
+      : "r"((uint32_t)v), "n"(kKeyBarrier), "n"(NTH)
       : "memory");
   return r != 0;
 }
@@ -654,23 +653,24 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
 }
 
 // ---------------------------------------------------------------------------
-// Per-channel key block of T tokens: warp w owns rows [w T/4, (w+1) T/4);
-// sixteen lanes cover one row (8 channels each), two rows per instruction.
-// The four warps' per-channel minima and maxima meet in shared memory; one
-// thread per channel then forms the scale, zero point and bracket.
+// Per-channel key block of T tokens, W warps: warp w owns rows
+// [w T/W, (w+1) T/W); sixteen lanes cover one row (8 channels each), two rows
+// per instruction. The warps' per-channel minima and maxima meet in shared
+// memory; one thread per channel then forms the scale, zero point and bracket.
 // ---------------------------------------------------------------------------
+template <int W>
 struct KeyScratch {
-  __half mn[kWarps][kHeadDim];
-  __half mx[kWarps][kHeadDim];
+  __half mn[W][kHeadDim];
+  __half mx[W][kHeadDim];
   float nz[kHeadDim], rlo[kHeadDim], rhi[kHeadDim], s[kHeadDim];
 };
 
-template <int BITS, int TB, bool OUTL>
+template <int BITS, int TB, bool OUTL, int W>
 __device__ __forceinline__ bool key_block(const unsigned char* tile, const TensorDev& K, int n,
-                                          int blk, bool ok, KeyScratch& ks, int warp, int lane,
+                                          int blk, bool ok, KeyScratch<W>& ks, int warp, int lane,
                                           unsigned char* rowbuf, int kout, uint16_t* ombuf) {
   constexpr int kLev = (1 << BITS) - 1;
-  constexpr int kRW = TB / kWarps;  // rows of this warp
+  constexpr int kRW = TB / W;  // rows of this warp
   constexpr int kIt = kRW / 2;      // rows per lane
   constexpr int kWords = Pack<BITS>::kWords;
   constexpr int PB = BITS == 3 ? 8 : BITS;
@@ -744,13 +744,13 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
     *reinterpret_cast<uint4*>(&ks.mn[warp][8 * o]) = make_uint4(bits(mn[0]), bits(mn[1]), bits(mn[2]), bits(mn[3]));
     *reinterpret_cast<uint4*>(&ks.mx[warp][8 * o]) = make_uint4(bits(mx[0]), bits(mx[1]), bits(mx[2]), bits(mx[3]));
   }
-  const bool all_ok = key_barrier_and(ok);
+  const bool all_ok = key_barrier_and<32 * W>(ok);
   bool fast = true;
-  if (all_ok) {
+  if (all_ok && threadIdx.x < kHeadDim) {
     const int c = threadIdx.x;  // one channel per thread
     __half m0 = ks.mn[0][c], m1 = ks.mx[0][c];
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) {
+    for (int w = 1; w < W; ++w) {
       m0 = __hmin(m0, ks.mn[w][c]);
       m1 = __hmax(m1, ks.mx[w][c]);
     }
@@ -774,7 +774,7 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
     ks.rhi[c] = rh;
     ks.s[c] = s;
   }
-  const bool all_fast = key_barrier_and(fast);
+  const bool all_fast = key_barrier_and<32 * W>(fast);
   if (!all_ok) return false;
   float nz[8], rl[8], rh[8];
 #pragma unroll
@@ -864,6 +864,9 @@ struct Geo {
   static constexpr bool kPerChannel = KMODE == KVQ_ASYM_PER_CHANNEL;
   static constexpr int kRows = (kPerChannel && TB > 64) ? TB : 64;  // rows per item
   static constexpr int kStageBytes = kRows * kHeadDim * 2;
+  // Warps per CTA: eight where a stage is a 128-token key block (32 KB; at
+  // most three CTAs fit an SM), four otherwise.
+  static constexpr int kW = kRows == 128 ? 8 : 4;
   // Two stages per CTA and at least five CTAs per SM (at most 102 registers
   // a thread) where the stages are 16 KB: the same bytes in flight per SM as
   // three stages at four CTAs, with a quarter more warps to cover the
@@ -871,28 +874,29 @@ struct Geo {
   // prefill). 32 KB stages (128-token key blocks) keep the register budget
   // of four CTAs.
   static constexpr int kStages = 2;
-  static constexpr int kMinBlocks = kStageBytes <= 16384 ? 5 : 4;
-  static constexpr size_t kScratch = kPerChannel ? sizeof(KeyScratch) : 0;
+  static constexpr int kMinBlocks = kStageBytes <= 16384 ? 5 : 3;
+  static constexpr size_t kScratch = kPerChannel ? sizeof(KeyScratch<kW>) : 0;
   static constexpr size_t kRowBuf = (KB == 3 || VB == 3) ? 4 * kHeadDim : 0;  // per warp, 3-bit repacking
   // per warp, the outlier masks of its key-block rows between the two passes
-  static constexpr size_t kOmBuf = (kPerChannel && OUTL) ? (size_t)TB / 8 * 32 * 2 : 0;
+  static constexpr size_t kOmBuf = (kPerChannel && OUTL) ? (size_t)TB / kW / 2 * 32 * 2 : 0;
   static constexpr size_t kCtl = 64;  // counters and barriers
   static constexpr size_t kBytes =
-      (size_t)kStages * kStageBytes + kScratch + kWarps * (kRowBuf + kOmBuf) + kCtl;
+      (size_t)kStages * kStageBytes + kScratch + kW * (kRowBuf + kOmBuf) + kCtl;
 };
 
 template <int KB, int KMODE, int TB, int VB, bool VSYM, bool OUTL>
-__global__ void __launch_bounds__(kThreads, (Geo<KB, KMODE, TB, VB, OUTL>::kMinBlocks))
+__global__ void __launch_bounds__(32 * Geo<KB, KMODE, TB, VB, OUTL>::kW, (Geo<KB, KMODE, TB, VB, OUTL>::kMinBlocks))
     prefill_fast_kernel(Args a) {
   using G = Geo<KB, KMODE, TB, VB, OUTL>;
   constexpr int S = G::kStages;
-  constexpr int RPW = G::kRows / kWarps;
+  constexpr int W = G::kW;
+  constexpr int RPW = G::kRows / W;
   extern __shared__ __align__(128) unsigned char smem[];
-  KeyScratch& ks = *reinterpret_cast<KeyScratch*>(smem + S * G::kStageBytes);
+  KeyScratch<W>& ks = *reinterpret_cast<KeyScratch<W>*>(smem + S * G::kStageBytes);
   unsigned char* rowbuf = smem + S * G::kStageBytes + G::kScratch + (size_t)(threadIdx.x >> 5) * G::kRowBuf;
-  uint16_t* ombuf = reinterpret_cast<uint16_t*>(smem + S * G::kStageBytes + G::kScratch + kWarps * G::kRowBuf +
+  uint16_t* ombuf = reinterpret_cast<uint16_t*>(smem + S * G::kStageBytes + G::kScratch + W * G::kRowBuf +
                                                 (size_t)(threadIdx.x >> 5) * G::kOmBuf);
-  unsigned char* ctl = smem + S * G::kStageBytes + G::kScratch + kWarps * (G::kRowBuf + G::kOmBuf);
+  unsigned char* ctl = smem + S * G::kStageBytes + G::kScratch + W * (G::kRowBuf + G::kOmBuf);
   int* cnt = reinterpret_cast<int*>(ctl);           // [S] warps done with a stage
   int* issued = reinterpret_cast<int*>(ctl + 16);   // [S] copies issued into a stage
   uint64_t* full = reinterpret_cast<uint64_t*>(ctl + 32);  // [S]
@@ -964,7 +968,7 @@ __global__ void __launch_bounds__(kThreads, (Geo<KB, KMODE, TB, VB, OUTL>::kMinB
     const unsigned char* tile = smem + (size_t)s * G::kStageBytes;
     if (r.kind == 0) {
       if constexpr (G::kPerChannel) {
-        if (!key_block<KB, TB, OUTL>(tile, a.k, r.n, r.idx, ok, ks, warp, lane, rowbuf, a.kout, ombuf))
+        if (!key_block<KB, TB, OUTL, W>(tile, a.k, r.n, r.idx, ok, ks, warp, lane, rowbuf, a.kout, ombuf))
           dead = true;
       }
     } else if (!dead) {
@@ -974,7 +978,7 @@ __global__ void __launch_bounds__(kThreads, (Geo<KB, KMODE, TB, VB, OUTL>::kMinB
         const uint4* s4 = reinterpret_cast<const uint4*>(a.ksrc + ((int64_t)r.n * a.seq_len + t0) * kHeadDim);
         uint4* d4 = reinterpret_cast<uint4*>(a.k.resid + (int64_t)r.n * a.k.resid_sstride);
         const int count = (a.seq_len - t0) * (kHeadDim / 8);
-        for (int i = tid; i < count; i += kThreads) d4[i] = s4[i];
+        for (int i = tid; i < count; i += 32 * W) d4[i] = s4[i];
       } else if (r.kind == 2) {
         rows_warp<KB, KMODE == KVQ_SYM_PER_TOKEN, RPW, OUTL>(tile, a.k, r.n, r.row0, r.nrows, warp, lane,
                                                              rowbuf, a.kout);
@@ -987,7 +991,7 @@ __global__ void __launch_bounds__(kThreads, (Geo<KB, KMODE, TB, VB, OUTL>::kMinB
       __syncwarp();
       if (lane == 0) {
         __threadfence_block();
-        if (atomicAdd(&cnt[s], 1) == kWarps - 1) {
+        if (atomicAdd(&cnt[s], 1) == W - 1) {
           cnt[s] = 0;
           __threadfence_block();
           const int nxt = it + S * stride;
@@ -1017,7 +1021,7 @@ cudaError_t launch_fast_t(const LayerDev& L, const __half* k, const __half* v, i
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)G::kBytes);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, G::kBytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * G::kW, G::kBytes);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
   }
@@ -1045,7 +1049,7 @@ cudaError_t launch_fast_t(const LayerDev& L, const __half* k, const __half* v, i
   if (total > 0x7fffffff) return cudaErrorInvalidValue;  // item index is 32-bit
   const int64_t slots = (int64_t)(sms > 0 ? sms : 1) * occ;
   const int grid = (int)(total < slots ? total : slots);
-  kern<<<grid, kThreads, G::kBytes, st>>>(a);
+  kern<<<grid, 32 * G::kW, G::kBytes, st>>>(a);
   return cudaGetLastError();
 }
 
