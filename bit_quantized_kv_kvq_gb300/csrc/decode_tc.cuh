@@ -629,8 +629,11 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && !OUTL) ? 4 : 3)
           const float mnew = up ? mt_ : m_run[nt];
           const float al = up ? exp2f(m_run[nt] - mnew) : 1.0f;
           l_run[nt] *= al;
+          // with one query head the zero-point sums are kept per token lane,
+          // so every lane takes head 0's factor (lane 0 holds it)
+          const float alz = one_head ? __shfl_sync(kFull, al, 0) : al;
   #pragma unroll
-          for (int q = 0; q < VGPR; ++q) zacc[nt][q] *= al;
+          for (int q = 0; q < VGPR; ++q) zacc[nt][q] *= alz;
   #pragma unroll
           for (int mv = 0; mv < C::MTV; ++mv)
   #pragma unroll

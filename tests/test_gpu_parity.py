@@ -364,6 +364,29 @@ def test_tensor_core_decode_outlier_counts(kout, gqa, vg):
     _run_case(wl, appends=2, check_every=1)
 
 
+@pytest.mark.parametrize("outliers", [0, 2])
+def test_one_head_late_max_rescale(outliers):
+    """One query head, one split: keys of every other 32-token tile scaled by
+    10, so a warp's running max jumps by more than the lazy threshold after
+    its first tile and every accumulator (zero-point sums kept per token
+    lane, outlier corrections) must follow the rescale."""
+    wl = replace(W.DENSE_SPARSE_128K, batch=1, num_q_heads=2, num_kv_heads=2, seq_len=333,
+                 outliers_per_row=outliers, dist="normal")
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(wl.seq_len)
+    big = (torch.arange(wl.seq_len) // 32) % 2 == 1
+    k[:, :, big] = k[:, :, big] * 10
+    q, _, _ = src.step(0)
+    cache = K.make_gpu_cache(wl, 340)
+    cache.prefill(0, k.cuda(), v.cuda())
+    cache.set_decode_splits(1)
+    oc = O.OracleCache(K.spec_of(wl), 2)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    ref = oc.decode(K.q_streams(q, wl), 0.088)
+    o = cache.decode(0, q.cuda(), 0.088).cpu().double().reshape(ref.shape).numpy()
+    K.assert_attention_close(o, ref)
+
+
 def test_tensor_core_decode_wide_value_scales():
     """Value groups whose scales span many powers of two (the fp16 operand
     keeps its precision through the running exponent)."""
