@@ -691,7 +691,7 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
       mx[j] = ninf;
     }
     bool tie = false;
-#pragma unroll(OUTL ? 2 : 4)
+#pragma unroll(OUTL ? 1 : 4)  // with outliers the body is long; code size matters more
     for (int i = 0; i < kIt; ++i) {
       const int row = warp * kRW + 2 * i + p;
       const uint4 raw = t4[row * 16 + o];
@@ -796,7 +796,7 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
   auto zat = [&](int i) { return ks.nz[8 * o + i]; };
   auto sat = [&](int i) { return ks.s[8 * o + i]; };
   auto rat = [&](int i) { return ks.rlo[8 * o + i]; };
-#pragma unroll 2
+#pragma unroll(OUTL ? 1 : 2)
   for (int i = 0; i < kIt; ++i) {
     const int row = warp * kRW + 2 * i + p;
     uint4 raw = t4[row * 16 + o];
