@@ -175,14 +175,19 @@ struct Cfg {
   static constexpr int KBIAS = 2 * 8 * 4;        // bias and score factor per head
   static constexpr int OUTS = OUTL ? (2 * kRows * H + H * kHeadDim) * 4 : 0;
   static constexpr int WSCR = FRAG + KBIAS + OUTS;
+  // With one query head (a run-time case of NT = 1) only head 0's output
+  // corrections and query rows are kept: about 13 KB less per CTA, which
+  // lets four outlier CTAs share an SM instead of three.
+  static constexpr int OUTS1 = OUTL ? kHeadDim * 4 : 0;
+  static constexpr int WSCR1 = FRAG + KBIAS + OUTS1;
   static constexpr size_t kMergeBytes = (size_t)kWarps * H * kHeadDim * 4;
   __host__ __device__ static constexpr int stage(int kout) { return STAGE0 + (OUTL ? 8 * kRows * kout : 0); }
   __host__ __device__ static constexpr size_t big(int kout) {
     return (size_t)kWarps * kStages * stage(kout) > kMergeBytes ? (size_t)kWarps * kStages * stage(kout)
                                                                  : kMergeBytes;
   }
-  __host__ __device__ static constexpr size_t smem_bytes(int kout) {
-    return big(kout) + (size_t)kWarps * WSCR + 2 * H * kHeadDim * 4 /*qf, qm*/ +
+  __host__ __device__ static constexpr size_t smem_bytes(int kout, bool one = false) {
+    return big(kout) + (size_t)kWarps * (one ? WSCR1 : WSCR) + 2 * (one ? 1 : H) * kHeadDim * 4 /*qf, qm*/ +
            kWarps * H * 2 * 4 /*m, l*/ + kWarps * kStages * 8 + 16;
   }
 };
@@ -190,10 +195,8 @@ struct Cfg {
 // 2^e as a float for -126 <= e <= 127.
 __device__ __forceinline__ float exp2i(int e) { return __uint_as_float((uint32_t)(127 + e) << 23); }
 
-// Outlier variants hold about 68 KB of shared memory, so three CTAs per SM
-// at most: they get the register budget of three.
 template <int KB, int VB, int VG, int NT, bool OUTL>
-__global__ void __launch_bounds__(kThreads, (NT == 1 && !OUTL) ? 4 : 3)
+__global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
     decode_tc_kernel(LayerDev L, DecodeArgs a) {
   using C = Cfg<KB, VB, VG, NT, OUTL>;
   constexpr int S = C::kStages;
@@ -213,15 +216,18 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && !OUTL) ? 4 : 3)
   const size_t big = C::big(kout);
   unsigned char* stages = smem;
   float* mo = reinterpret_cast<float*>(smem);  // merge area, after the main loop: [warps][H][128]
-  unsigned char* wscr = smem + big + (size_t)warp * C::WSCR;
+  const bool one_head = NT == 1 && G == 1;  // warp-uniform
+  const int HQ = one_head ? 1 : H;           // query rows and output-correction rows kept
+  const size_t wsz = one_head ? C::WSCR1 : C::WSCR;
+  unsigned char* wscr = smem + big + (size_t)warp * wsz;
   uint32_t* frag = reinterpret_cast<uint32_t*>(wscr);           // [32][NT][8][2]
   float* kbias = reinterpret_cast<float*>(wscr + C::FRAG);       // [8] bias, [8] score factor
   float* ocs = reinterpret_cast<float*>(wscr + C::FRAG + C::KBIAS);  // [32 rows][H] score corrections
   float* pst = ocs + kRows * H;                                   // [32 rows][H] probabilities
-  float* ocr = pst + kRows * H;                                   // [H][128] output corrections
-  float* qf = reinterpret_cast<float*>(smem + big + (size_t)kWarps * C::WSCR);  // [H][128]
-  float* qm = qf + H * kHeadDim;                                  // [H][128] qf * 2^-shift
-  float* ml = qm + H * kHeadDim;                                  // [warps][H][2]
+  float* ocr = one_head ? ocs : pst + kRows * H;                  // [HQ][128] output corrections
+  float* qf = reinterpret_cast<float*>(smem + big + (size_t)kWarps * wsz);  // [HQ][128]
+  float* qm = qf + HQ * kHeadDim;                                 // [HQ][128] qf * 2^-shift
+  float* ml = qm + HQ * kHeadDim;                                 // [warps][H][2]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ml + kWarps * H * 2);
 
   const int len = a.length, kq = a.k_quant_len;
@@ -238,7 +244,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && !OUTL) ? 4 : 3)
   const unsigned char* kmeta = L.k.meta + (int64_t)n * L.k.meta_sstride;
   const unsigned char* vmeta = L.v.meta + (int64_t)n * L.v.meta_sstride;
 
-  for (int i = tid; i < H * kHeadDim; i += kThreads) {
+  for (int i = tid; i < HQ * kHeadDim; i += kThreads) {
     const int h = i >> 7, c = i & 127;
     const float v = h < G ? __half2float(a.q[((int64_t)b * a.num_q_heads + hq0 + h) * kHeadDim + c]) *
                                 a.scale_log2
@@ -248,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && !OUTL) ? 4 : 3)
   }
   for (int i = lane; i < 32 * NT * 16; i += 32) frag[i] = 0u;
   if (OUTL)
-    for (int i = lane; i < H * kHeadDim; i += 32) ocr[i] = 0.0f;
+    for (int i = lane; i < HQ * kHeadDim; i += 32) ocr[i] = 0.0f;
   uint64_t* wb = bars + warp * S;
   if (lane == 0) {
     for (int s = 0; s < S; ++s) mbar_init(&wb[s], 1);
@@ -333,7 +339,6 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && !OUTL) ? 4 : 3)
   float sc[NT][2][2], mx_n[NT], p[NT][2][2];
   float vsf[VGPR];  // 2^(6 - ev[q])
   uint32_t pw[VGPR];
-  const bool one_head = NT == 1 && G == 1;  // warp-uniform
   // One query head: value-outlier corrections p_t (x - z_t) of the lane's
   // tokens are summed in registers for the first four channels the lane
   // meets (outliers gather in a few channels, which then stay in registers
@@ -645,8 +650,9 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && !OUTL) ? 4 : 3)
             for (int hh = 0; hh < 4; ++hh) {
               const float alh = __shfl_sync(kFull, al, hh);
               const int h = 4 * nt + hh;
+              if (h < HQ)
   #pragma unroll
-              for (int k = 0; k < 4; ++k) ocr[h * kHeadDim + lane + 32 * k] *= alh;
+                for (int k = 0; k < 4; ++k) ocr[h * kHeadDim + lane + 32 * k] *= alh;
             }
             if (one_head) {
               const float al0 = __shfl_sync(kFull, al, 0);
@@ -1040,7 +1046,7 @@ __global__ void __launch_bounds__(kThreads, (NT == 1 && !OUTL) ? 4 : 3)
 template <int KB, int VB, int VG, int NT, bool OUTL>
 cudaError_t launch_t(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<KB, VB, VG, NT, OUTL>;
-  const size_t sm = C::smem_bytes(OUTL ? L.outliers : 0);
+  const size_t sm = C::smem_bytes(OUTL ? L.outliers : 0, NT == 1 && a.gqa == 1);
   auto kern = decode_tc_kernel<KB, VB, VG, NT, OUTL>;
   static bool attr_set = false;
   if (!attr_set) {  // room for the most outliers a row may hold
