@@ -476,7 +476,7 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
   const int sw = q >> 2;
   const int lpg = T.group >> 4;  // lanes per group (groups of 16 .. 128 channels)
   const int per_row = kHeadDim / T.group;
-#pragma unroll(OUTL ? 1 : 2)  // outlier selection makes the body long enough
+#pragma unroll(OUTL ? 1 : 2)  // with outliers the body is long: code size matters more
   for (int it = 0; it < RPW / 4; ++it) {
     const int lr = warp * RPW + it * 4 + rr;
     const bool live = lr < nrows;
