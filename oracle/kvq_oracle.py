@@ -25,8 +25,8 @@ Precision. The codec decides integer codes, so it runs in fp32 with IEEE
 round-to-nearest-even at every step (numpy float32 ufuncs do not contract
 to FMA): a code is an integer decided by floating point, and both sides take
 that decision in the same precision. Dequantization and attention run in
-fp64. Readings of points the pages leave open are listed in the design doc
-(readings R1..R12) and restated where they are used.
+fp64. Where the pages leave a point open, the reading taken is numbered
+(R1, R2, ...) and stated in the function that uses it.
 
 Every function here is pinned by ``tests/test_oracle_pins.py`` against
 values the pages print, closed forms, brute force or library routines.
