@@ -3,7 +3,10 @@
 // The combine merges per-split partials (m_i, l_i, o_i), with m in log2
 // units, by the log-sum-exp rule: M = max m_i, L = sum l_i 2^(m_i - M),
 // o = sum o_i 2^(m_i - M) / L.
+#include <cstring>
+
 #include "decode_impl.cuh"
+#include "decode_pipe.cuh"
 
 namespace kvq {
 namespace {
@@ -57,6 +60,83 @@ static cudaError_t launch_decode_tc(const LayerDev& L, const DecodeArgs& a, cuda
     case 84: return launch_decode_tc_k84(L, a, st);
     default: return launch_decode_tc_k88(L, a, st);
   }
+}
+
+cudaError_t launch_decode_pipe_k33(const LayerDev& L, const pipe::Args& a, cudaStream_t st);
+cudaError_t launch_decode_pipe_k44(const LayerDev& L, const pipe::Args& a, cudaStream_t st);
+cudaError_t launch_decode_pipe_k48(const LayerDev& L, const pipe::Args& a, cudaStream_t st);
+cudaError_t launch_decode_pipe_k84(const LayerDev& L, const pipe::Args& a, cudaStream_t st);
+cudaError_t launch_decode_pipe_k88(const LayerDev& L, const pipe::Args& a, cudaStream_t st);
+
+// The stream-K kernel puts the query heads of a kv-head on the mma rows
+// (heads x hi/lo): with 8 heads every row and lane is used and P leaves QK^T
+// in PV's operand layout. With fewer heads most rows and softmax lanes would
+// idle, so 1, 2 and 4 heads per kv-head use the token-row kernels of
+// decode_tc.cuh instead.
+bool decode_pipe_supported(const LayerDev& L, int gqa) {
+  if (gqa != 8) return false;
+  if (L.k.mode != KVQ_ASYM_PER_CHANNEL || L.v.mode != KVQ_ASYM_PER_TOKEN) return false;
+  if (L.k.group != 64 && L.k.group != 128 && L.k.group != 256) return false;
+  switch (L.k.bits * 10 + L.v.bits) {
+    case 33: return L.v.group == 128;
+    case 44: case 48: case 84: case 88: return L.v.group == 64 || L.v.group == 128;
+    default: return false;
+  }
+}
+
+// Partition of the key blocks of all streams over `ctas` CTAs: CTA c takes
+// blocks [c N / P, (c + 1) N / P). A stream of cps blocks meets at most
+// ceil(P / streams) + 1 CTAs, which bounds the partial rows per stream.
+PipePlan plan_decode_pipe(const LayerDev& L, int len, int gqa, int sm_count, int ctas_override) {
+  PipePlan p;
+  const int T = L.k.group;
+  p.cps = (len + T - 1) / T;
+  p.n_chunks = (long long)L.n_streams * p.cps;
+  int P = sm_count > 0 ? sm_count : 1;
+  if (ctas_override > 0 && ctas_override < P) P = ctas_override;
+  if ((long long)P > p.n_chunks) P = (int)p.n_chunks;
+  if (P < 1) P = 1;
+  p.ctas = P;
+  p.jmax = (P + L.n_streams - 1) / L.n_streams + 1;
+  p.ws_bytes = (size_t)L.n_streams * p.jmax * gqa * pipe::kPartRow * 4;
+  return p;
+}
+
+size_t decode_pipe_workspace_max(const LayerDev& L, int gqa, int sm_count) {
+  const int P = sm_count > 0 ? sm_count : 1;
+  const int jmax = (P + L.n_streams - 1) / L.n_streams + 1;
+  return (size_t)L.n_streams * jmax * gqa * pipe::kPartRow * 4;
+}
+
+cudaError_t launch_decode_pipe(const LayerDev& L, const DecodeArgs& d, const PipePlan& p, cudaStream_t st) {
+  pipe::Args a;
+  std::memset(&a, 0, sizeof a);
+  a.q = d.q;
+  a.out = d.out;
+  a.part = d.part_o;
+  a.counters = L.counters;
+  a.out_dtype = d.out_dtype;
+  a.num_q_heads = d.num_q_heads;
+  a.H = d.gqa;
+  a.scale_log2 = d.scale_log2;
+  a.length = d.length;
+  a.kq = d.k_quant_len;
+  a.T = L.k.group;
+  a.cps = p.cps;
+  a.n_chunks = p.n_chunks;
+  a.P = p.ctas;
+  a.jmax = p.jmax;
+  a.kout = L.outliers;
+  cudaError_t e;
+  switch (L.k.bits * 10 + L.v.bits) {
+    case 33: e = launch_decode_pipe_k33(L, a, st); break;
+    case 44: e = launch_decode_pipe_k44(L, a, st); break;
+    case 48: e = launch_decode_pipe_k48(L, a, st); break;
+    case 84: e = launch_decode_pipe_k84(L, a, st); break;
+    default: e = launch_decode_pipe_k88(L, a, st); break;
+  }
+  if (e == cudaSuccess) count_launches(1);
+  return e;
 }
 
 bool decode_supported(const LayerDev& L, int gqa) {

@@ -1,0 +1,139 @@
+// Host side of the stream-K decode kernel (decode_pipe.cuh): work partition,
+// shared-memory plan, tensor maps of the code arrays, launch. The including
+// translation unit picks the key/value code widths with KVQ_PIPE_KB and
+// KVQ_PIPE_VB.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "decode_pipe.cuh"
+
+namespace kvq {
+namespace pipe {
+
+inline int round_up_i(int x, int m) { return (x + m - 1) / m * m; }
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// Code rows of one tensor as a uint8 tensor [stream][row][byte]; a box is
+// `box_rows` whole rows, written to shared memory with the bank swizzle of the
+// row width (64 or 128 bytes).
+inline cudaError_t encode_rows(CUtensorMap* m, const void* base, int row_bytes, int cap, int n_streams,
+                               int64_t stream_bytes, int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)cap, (cuuint64_t)n_streams};
+  const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)stream_bytes};
+  const cuuint32_t box[3] = {(cuuint32_t)row_bytes, (cuuint32_t)box_rows, 1u};
+  const cuuint32_t es[3] = {1u, 1u, 1u};
+  const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+constexpr int kSmemMax = 232448;  // dynamic shared memory per CTA on sm_103a (227 KB)
+
+template <int KB, int VB, int VG, bool OUTL>
+struct Plan {
+  static constexpr int KROW = 4 * Pack<KB>::kWords, VROW = 4 * Pack<VB>::kWords;
+  static constexpr int VGPR = kHeadDim / VG;
+  static constexpr int UT = 32;
+
+  // Fills the shared-memory layout of `a` (H, kout, T set) and returns the
+  // dynamic shared memory the launch needs, or 0 if it does not fit.
+  static int layout(Args& a) {
+    a.UT = UT;
+    a.U = a.T / UT;
+    const int H = a.H, kout = OUTL ? a.kout : 0;
+    a.kc_bytes = UT * KROW;
+    a.vc_bytes = UT * VROW;
+    a.vm_bytes = UT * VGPR * 4;
+    const bool swz = KB != 3 || VB != 3;
+    a.off_vc = round_up_i(a.kc_bytes, VB != 3 ? 1024 : 128);
+    a.off_km = round_up_i(a.off_vc + a.vc_bytes, 128);
+    a.off_vm = a.off_km + kHeadDim * 4;
+    a.off_out = round_up_i(a.off_vm + a.vm_bytes, 128);
+    a.stage_bytes = round_up_i(a.off_out + (OUTL ? 4 * UT * kout * 2 : 0), swz ? 1024 : 128);
+    a.w_qn = 0;
+    a.w_frag = round_up_i(H * kHeadDim * 4, 16);
+    // fragment rows of heads < H; with outliers and several heads the area
+    // also holds a [32 tokens][8 heads] float exchange
+    const int frag_bytes = 4 * H * kFragRow * 16;
+    a.w_eq = a.w_frag + (OUTL && H > 1 && frag_bytes < 32 * kHMax * 4 ? 32 * kHMax * 4 : frag_bytes);
+    a.w_kz = a.w_eq + 32;
+    a.w_ocr = a.w_kz + (OUTL ? kHeadDim * 4 : 0);
+    a.warp_bytes = round_up_i(a.w_ocr + (OUTL ? H * kHeadDim * 4 : 0), 128);
+    a.slot_bytes = round_up_i((H * kHeadDim + 2 * kHMax) * 4, 128);
+    const int fixed = 1024 /* base alignment */ + kCons * a.warp_bytes + 2 * a.slot_bytes + 128;
+    int ns = (kSmemMax - fixed) / (a.stage_bytes + 16);  // + barrier and last-issue word per stage
+    if (ns > 64) ns = 64;
+    ns -= ns % a.U;  // a stage's next unit is then a whole number of key blocks ahead
+    if (ns < a.U) return 0;  // at least one key block of stages (warps then take turns)
+    a.ns = ns;
+    a.ring_bytes = ns * a.stage_bytes;
+    return fixed + a.ring_bytes + 16 * ns;
+  }
+};
+
+template <int KB, int VB, int VG, bool OUTL>
+cudaError_t launch_t(const LayerDev& L, Args a, cudaStream_t st) {
+  using PL = Plan<KB, VB, VG, OUTL>;
+  const int smem = PL::layout(a);
+  if (smem == 0) return cudaErrorInvalidConfiguration;
+  Maps maps;
+  std::memset(&maps, 0, sizeof maps);
+  if (KB != 3) {
+    cudaError_t e = encode_rows(&maps.k, L.k.codes, PL::KROW, L.capacity, L.n_streams,
+                                L.k.codes_sstride * 4, PL::UT);
+    if (e != cudaSuccess) return e;
+  }
+  if (VB != 3) {
+    cudaError_t e = encode_rows(&maps.v, L.v.codes, PL::VROW, L.capacity, L.n_streams,
+                                L.v.codes_sstride * 4, PL::UT);
+    if (e != cudaSuccess) return e;
+  }
+  auto kern = decode_pipe_kernel<KB, VB, VG, OUTL>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  kern<<<a.P, kThreads, smem, st>>>(maps, L, a);
+  return cudaGetLastError();
+}
+
+}  // namespace pipe
+
+#define KVQ_PIPE_NAME3(a, b, c) a##b##c
+#define KVQ_PIPE_NAME(b, c) KVQ_PIPE_NAME3(launch_decode_pipe_k, b, c)
+
+cudaError_t KVQ_PIPE_NAME(KVQ_PIPE_KB, KVQ_PIPE_VB)(const LayerDev& L, const pipe::Args& a, cudaStream_t st) {
+  constexpr int KB = KVQ_PIPE_KB, VB = KVQ_PIPE_VB;
+  const bool outl = L.outliers > 0;
+  if (VB == 3 || L.v.group == 128)
+    return outl ? pipe::launch_t<KB, VB, 128, true>(L, a, st) : pipe::launch_t<KB, VB, 128, false>(L, a, st);
+  if constexpr (VB != 3)
+    return outl ? pipe::launch_t<KB, VB, 64, true>(L, a, st) : pipe::launch_t<KB, VB, 64, false>(L, a, st);
+  return cudaErrorNotSupported;
+}
+
+}  // namespace kvq

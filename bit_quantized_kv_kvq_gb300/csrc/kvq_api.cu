@@ -58,6 +58,7 @@ struct Plan {
   int capacity = 0;
   int64_t n_streams = 0;
   TensorPlan k, v;
+  int64_t ctr_off = 0;  // per layer: uint32 split-merge counters [n_streams]
   int64_t layer_bytes = 0;
   int64_t header_bytes = 256;
   int64_t total = 0;
@@ -142,6 +143,8 @@ Plan make_plan(const kvq_config& c) {
   int64_t cursor = 0;
   plan_tensor(c, p.capacity, true, &cursor, &p.k);
   plan_tensor(c, p.capacity, false, &cursor, &p.v);
+  p.ctr_off = cursor;
+  cursor = round_up(cursor + p.n_streams * 4, 256);
   p.layer_bytes = cursor;
   p.total = p.header_bytes + p.layer_bytes * c.num_layers;
   return p;
@@ -195,6 +198,8 @@ kvq::LayerDev layer_dev(const kvq_cache* h, int layer) {
   L.capacity = h->plan.capacity;
   L.outliers = h->cfg.outliers_per_row;
   L.status = reinterpret_cast<uint32_t*>(h->base);
+  L.counters = reinterpret_cast<uint32_t*>(h->base + h->plan.header_bytes +
+                                           (int64_t)layer * h->plan.layer_bytes + h->plan.ctr_off);
   return L;
 }
 
@@ -353,6 +358,14 @@ kvq_status kvq_append_quantize(kvq_cache* h, int32_t layer, const void* k, const
 kvq_status kvq_decode_workspace_bytes(const kvq_cache* h, int32_t num_q_heads, size_t* bytes) {
   if (!h || !bytes) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
   if (num_q_heads < 1) return fail(KVQ_ERR_INVALID_ARG, "num_q_heads must be >= 1");
+  const int hkv = h->cfg.num_kv_heads;
+  if (num_q_heads % hkv == 0) {
+    kvq::LayerDev L = layer_dev(h, 0);
+    if (kvq::decode_pipe_supported(L, num_q_heads / hkv)) {
+      *bytes = kvq::decode_pipe_workspace_max(L, num_q_heads / hkv, h->sm_count);
+      return KVQ_OK;
+    }
+  }
   const int max_splits = h->plan.capacity / kvq::kTile;  // one tile per split at most
   *bytes = workspace_for(h, num_q_heads, max_splits);
   return KVQ_OK;
@@ -383,6 +396,21 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
   std::memset(&a, 0, sizeof a);
   a.gqa = gqa;
   a.num_q_heads = num_q_heads;
+  if (kvq::decode_pipe_supported(L, gqa)) {
+    const kvq::PipePlan pp = kvq::plan_decode_pipe(L, len, gqa, h->sm_count, h->splits_override);
+    if (ws_bytes < pp.ws_bytes)
+      return fail(KVQ_ERR_BUFFER_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, pp.ws_bytes);
+    a.q = static_cast<const __half*>(q);
+    a.out = out;
+    a.out_dtype = out_dtype;
+    a.scale_log2 = softmax_scale * 1.4426950408889634f;
+    a.length = len;
+    a.k_quant_len = k_quant_len(h->cfg, len);
+    a.part_o = static_cast<float*>(workspace);
+    cudaError_t e = kvq::launch_decode_pipe(L, a, pp, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return KVQ_OK;
+  }
   int occ = 0;
   a.occupancy_out = &occ;
   cudaError_t e = kvq::launch_decode(L, a, static_cast<cudaStream_t>(stream));
@@ -474,6 +502,12 @@ kvq_status kvq_cache_status(kvq_cache* h, void* stream, uint32_t* word) {
   if (w != 0) {
     e = cudaMemset(h->base, 0, sizeof w);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemset status");
+    // a decode that gave up may have left split-merge counters set
+    for (int l = 0; l < h->cfg.num_layers; ++l) {
+      e = cudaMemset(h->base + h->plan.header_bytes + (int64_t)l * h->plan.layer_bytes + h->plan.ctr_off, 0,
+                     (size_t)h->plan.n_streams * 4);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaMemset counters");
+    }
   }
   if (word) *word = w;
   if (w & kvq::kStatusTimeout) return fail(KVQ_ERR_TIMEOUT, "a bounded device wait gave up (status 0x%x)", w);

@@ -44,6 +44,7 @@ struct LayerDev {
   int capacity;
   int outliers;         // per row
   uint32_t* status;
+  uint32_t* counters;   // [n_streams] split-merge counters of the layer, zero between calls
 };
 
 // Prefill of seq_len tokens: k, v fp16 [n][seq_len][D].
@@ -74,6 +75,20 @@ struct DecodeArgs {
 cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);
 
 bool decode_supported(const LayerDev& L, int gqa);
+
+// Stream-K decode (decode_pipe.cuh): per-channel keys and asymmetric per-token
+// values at 3/3, 4/4, 4/8, 8/4 or 8/8 bits, 1, 2, 4 or 8 query heads per kv-head.
+struct PipePlan {
+  int ctas;             // persistent CTAs (at most one per SM)
+  int jmax;             // partial rows per stream
+  int cps;              // key blocks per stream
+  long long n_chunks;   // key blocks of all streams
+  size_t ws_bytes;      // workspace: partials
+};
+bool decode_pipe_supported(const LayerDev& L, int gqa);
+PipePlan plan_decode_pipe(const LayerDev& L, int len, int gqa, int sm_count, int ctas_override);
+size_t decode_pipe_workspace_max(const LayerDev& L, int gqa, int sm_count);
+cudaError_t launch_decode_pipe(const LayerDev& L, const DecodeArgs& a, const PipePlan& p, cudaStream_t stream);
 bool decode_mha_supported(const LayerDev& L);
 cudaError_t launch_decode_mha(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);
 bool decode_gqa_supported(const LayerDev& L, int gqa);

@@ -171,24 +171,51 @@ def test_errors_are_reported_not_raised_on_device():
 
 
 def test_launch_counter_matches_the_work_enqueued():
-    """prefill, append and decode enqueue one kernel each, plus the split
-    combine when the decode was split."""
+    """prefill, append and decode enqueue one kernel each. The stream-K decode
+    (per-channel keys, 8 query heads per kv-head) merges its splits inside its
+    one kernel; the split-K decodes add the split combine when split."""
     import bit_quantized_kv_kvq_gb300 as kvq
-    wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=4, num_kv_heads=4, seq_len=300)
+    for kmode, hq, extra_split in ((W.ASYM_PER_CHANNEL, 32, 1), (W.ASYM_PER_TOKEN, 4, 2)):
+        wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=hq, num_kv_heads=4, seq_len=300, k_mode=kmode,
+                     k_group=64 if kmode == W.ASYM_PER_CHANNEL else 32)
+        src = LayerSource(wl, 0, device="cpu")
+        k, v = src.kv(wl.seq_len)
+        q, k1, v1 = src.step(0)
+        cache = K.make_gpu_cache(wl, 400)
+        n0 = kvq.kernel_launches()
+        cache.prefill(0, k.cuda(), v.cuda())
+        cache.append(0, k1.cuda(), v1.cuda())
+        assert kvq.kernel_launches() - n0 == 2
+        for splits, extra in ((1, 1), (3, extra_split)):
+            cache.set_decode_splits(splits)
+            n1 = kvq.kernel_launches()
+            cache.decode(0, q.cuda(), 0.1)
+            assert kvq.kernel_launches() - n1 == extra
+        torch.cuda.synchronize()
+        assert cache.status() == 0
+
+
+@pytest.mark.parametrize("ctas", [1, 2, 3, 5, 8, 13, 0])
+@pytest.mark.parametrize("seq,batch,hkv", [(70, 3, 4), (1000, 1, 2), (333, 2, 3)])
+def test_stream_k_partitions(ctas, seq, batch, hkv):
+    """The stream-K decode (per-channel keys, 8 query heads per kv-head) cuts
+    the key blocks of all streams into one range per CTA: one CTA holding many whole streams, streams cut across several
+    CTAs, and ranges that start and end mid-stream must all agree with the
+    oracle (the split-merge counters are reused across the calls)."""
+    wl = replace(W.LLAMA8B_FULL, num_layers=1, batch=batch, num_kv_heads=hkv, num_q_heads=8 * hkv,
+                 seq_len=seq)
     src = LayerSource(wl, 0, device="cpu")
-    k, v = src.kv(wl.seq_len)
-    q, k1, v1 = src.step(0)
-    cache = K.make_gpu_cache(wl, 400)
-    n0 = kvq.kernel_launches()
+    k, v = src.kv(seq)
+    cache = K.make_gpu_cache(wl, seq + 2)
     cache.prefill(0, k.cuda(), v.cuda())
-    cache.append(0, k1.cuda(), v1.cuda())
-    assert kvq.kernel_launches() - n0 == 2
-    for splits, extra in ((1, 1), (3, 2)):
-        cache.set_decode_splits(splits)
-        n1 = kvq.kernel_launches()
-        cache.decode(0, q.cuda(), 0.1)
-        assert kvq.kernel_launches() - n1 == extra
-    torch.cuda.synchronize()
+    oc = O.OracleCache(K.spec_of(wl), wl.batch * wl.num_kv_heads)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    cache.set_decode_splits(ctas)
+    for call in range(3):
+        q, _, _ = src.step(50 + call)
+        ref = oc.decode(K.q_streams(q, wl), 0.088)
+        o = cache.decode(0, q.cuda(), 0.088).cpu().double().reshape(ref.shape).numpy()
+        K.assert_attention_close(o, ref, where="ctas %d call %d" % (ctas, call))
     assert cache.status() == 0
 
 

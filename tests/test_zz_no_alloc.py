@@ -53,8 +53,10 @@ def test_static_scratch_matches_workspace_path(wl):
 
 
 def test_static_scratch_rejects_oversized_calls():
-    # 512 rows x many splits of fp32 partials is far above the 4 MiB maximum
-    wl = replace(W.LLAMA7B_16K, batch=16, num_q_heads=32, num_kv_heads=32, seq_len=4096)
+    # per-token keys decode through split partials: 512 rows x 64 splits of
+    # fp32 partials is far above the 4 MiB maximum
+    wl = replace(W.LLAMA7B_16K, batch=16, num_q_heads=32, num_kv_heads=32, seq_len=4096,
+                 k_mode=W.ASYM_PER_TOKEN, k_group=32)
     cache = K.make_gpu_cache(wl, wl.seq_len)
     src = LayerSource(wl, 0, device="cuda")
     k, v = src.kv(wl.seq_len)
