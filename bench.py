@@ -1,17 +1,23 @@
-"""Benchmark of the whole hot path on one GB300 (or N replicas).
+"""Benchmark of the hot path on one GB300 (or N replicas).
 
-One step = prefill quantize of the layer's K/V (all streams, full context),
-append of one token per stream, and fused dequant decode attention of one
-query token per (batch, query head) over the whole cache -- every step of the
-codec and of the attention, through the C ABI. Inputs are seeded synthetic
-fp16 tensors already resident in HBM; they are larger than L2 (129 MB), so no
-L2 flush is needed between timed steps.
+The default workload is the full 8B-shaped decode: 32 layers x 8 kv-heads (32
+query heads), head_dim 128, batch 1, a 131072-token context prefill-quantized
+into the cache (4-bit per-channel keys, 8-bit per-token values), then decode
+steps that each append one token and run fused dequant decode attention on
+every layer. One timed step = append on all layers, then decode attention on
+all layers, through the C ABI, with inputs resident in HBM. Each layer's
+packed cache (218 MB) is larger than L2 (129 MB), so consecutive decodes read
+from HBM; single-layer workloads flush L2 between steps (outside the decode's
+own timing).
 
-Prints one JSON line (rank 0). ``value`` is the whole-step algorithmic
-throughput in GB/s (bytes read + written by prefill, append and decode per
-step, divided by the step time); the line also carries the decode-attention
-and quantize throughputs, the roofline of the dominant kernel, clocks, the
-end-to-end number through host buffers and the CPU oracle baseline.
+Prints one JSON line (rank 0). ``value`` is the fused dequant decode-attention
+throughput in GB/s: the algorithmic bytes the decode attention of all layers
+reads and writes per step (packed codes, fp16 scales and zero points, outlier
+lists, fp16 residual keys, q, output), divided by the decode time of the step
+(CUDA events around the block of decode calls). The line also carries the
+whole-step time, the prefill quantize and append throughputs, the roofline of
+the decode kernel, clocks, the end-to-end number through host buffers and the
+CPU oracle baseline.
 
 ``--impl reference`` times the CPU oracle instead (the reference arm).
 Under torchrun (N > 1) each rank runs an independent replica (the path has
@@ -38,7 +44,7 @@ from bit_quantized_kv_kvq_gb300 import accounting as A  # noqa: E402
 from bit_quantized_kv_kvq_gb300 import workloads as W  # noqa: E402
 
 METRIC = "fused dequant decode-attention KV GB/s (% of GB300 HBM peak); quantize GB/s"
-DEFAULT_WORKLOAD = W.LLAMA7B_16K.name
+DEFAULT_WORKLOAD = W.LLAMA8B_FULL.name
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -99,13 +105,23 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def gpu_id(device):
+    """nvidia-smi's name for a torch device: its UUID (the torch index is a
+    logical one under CUDA_VISIBLE_DEVICES and need not match nvidia-smi's)."""
+    try:
+        u = str(torch.cuda.get_device_properties(device).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return str(device.index)
+
+
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
+    def __init__(self, gpu):
+        self.gpu = gpu
         self.proc = None
         self.path = None
 
@@ -147,7 +163,8 @@ class ClockSampler:
             except Exception:
                 pass
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+            return {"gpu": str(self.gpu), "sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"],
+                    "samples": 0}
 
         def num(x):
             try:
@@ -162,131 +179,227 @@ class ClockSampler:
         for i, nm in enumerate(names):
             if any(r[5 + i].lower().startswith("active") for r in rows):
                 reasons.append(nm)
-        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(num(r[2]) for r in rows),
-                "reasons": reasons, "samples": len(rows)}
+        return {"gpu": rows[0][0], "sm_mhz": statistics.median(load),
+                "sm_max_mhz": max(num(r[2]) for r in rows), "reasons": reasons, "samples": len(rows)}
 
 
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 
+def gbs(b, ms):
+    return b / (ms * 1e-3) / 1e9
+
+
+class Model:
+    """The workload's layers in one packed cache: every layer prefilled with
+    its seeded context, then decode steps (append one token per stream and
+    layer, decode attention of every layer)."""
+
+    def __init__(self, wl, device, seed, max_steps):
+        import bit_quantized_kv_kvq_gb300 as kvq
+        from bit_quantized_kv_kvq_gb300.synth import LayerSource
+        self.wl, self.device = wl, device
+        self.S = wl.seq_len
+        self.cache = kvq.QuantizedKVCache(wl.num_layers, wl.batch, wl.num_kv_heads, wl.head_dim,
+                                          self.S + max_steps, wl.k_bits, wl.v_bits, wl.k_mode,
+                                          wl.v_mode, wl.k_group, wl.v_group, wl.outliers_per_row,
+                                          device=device)
+        self.src = [LayerSource(wl, l, device=device, seed=seed) for l in range(wl.num_layers)]
+        self.ws = self.cache.workspace(wl.num_q_heads)
+        self.scale = 1.0 / math.sqrt(wl.head_dim)
+        self.out = torch.empty((wl.num_layers, wl.batch, wl.num_q_heads, wl.head_dim),
+                               dtype=torch.float32, device=device)
+        # per step and layer: (q, k1, v1), drawn ahead of time
+        self.inputs = [[self.src[l].step(st) for l in range(wl.num_layers)] for st in range(max_steps)]
+
+    def prefill_all(self):
+        """Prefills every layer; returns the K/V of layer 0 (kept for the
+        quantize timing)."""
+        kv0 = None
+        for l in range(self.wl.num_layers):
+            k, v = self.src[l].kv(self.S)
+            self.cache.prefill(l, k, v)
+            if l == 0:
+                kv0 = (k, v)
+            else:
+                del k, v
+        return kv0
+
+    def length(self):
+        return self.cache.length(0)
+
+
+def l2_flush_buffers(device):
+    """Two 256 MB buffers: writing one and then reading it back into the other
+    leaves L2 (129 MB) holding clean lines unrelated to the cache."""
+    a = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    b = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+
+    def flush(i):
+        a.fill_(i & 255)
+        b.copy_(a)
+    return flush
+
+
 def run_gpu(args, wl, rank, world, device):
     import bit_quantized_kv_kvq_gb300 as kvq
-    from bit_quantized_kv_kvq_gb300.synth import LayerSource
 
     torch.cuda.set_device(device)
-    S = wl.seq_len
-    cache = kvq.QuantizedKVCache(1, wl.batch, wl.num_kv_heads, wl.head_dim, S + 1, wl.k_bits,
-                                 wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group, wl.v_group,
-                                 wl.outliers_per_row, device=device)
-    src = LayerSource(wl, 0, device=device, seed=replica_seed(wl, rank))
-    k, v = src.kv(S)
-    q, k1, v1 = src.step(0)
-    out = torch.empty((wl.batch, wl.num_q_heads, wl.head_dim), dtype=torch.float32, device=device)
-    ws = cache.workspace(wl.num_q_heads)
-    scale = 1.0 / math.sqrt(wl.head_dim)
     stream = torch.cuda.current_stream(device)
+    L = wl.num_layers
+    steps, warm = args.steps, args.warmup
+    model = Model(wl, device, replica_seed(wl, rank), warm + steps + 14)
+    cache, ws, scale, out = model.cache, model.ws, model.scale, model.out
+    k0, v0 = model.prefill_all()
+    torch.cuda.synchronize(device)
+    assert cache.status() == 0
+    # each layer's cache larger than L2 makes consecutive decodes cold; a
+    # single layer that fits in L2 gets a flush before each step
+    per_layer = A.cache_read_bytes(wl, model.S)
+    need_flush = L == 1 or per_layer < 2 * (129 << 20)
+    flush = l2_flush_buffers(device) if need_flush else None
 
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
-        cache.prefill(0, k, v)
-        if ev:
-            ev[1].record(stream)
-        cache.append(0, k1, v1)
+    def decode_step(st, ev=None):
+        if flush is not None:
+            flush(st)
         if ev:
             ev[2].record(stream)
-        cache.decode(0, q, scale, out=out, workspace=ws)
+        for l in range(L):
+            _, k1, v1 = model.inputs[st][l]
+            cache.append(l, k1, v1)
         if ev:
-            ev[3].record(stream)
+            ev[0].record(stream)
+        for l in range(L):
+            q, _, _ = model.inputs[st][l]
+            cache.decode(l, q, scale, out=out[l], workspace=ws)
+        if ev:
+            ev[1].record(stream)
 
-    for _ in range(args.warmup):
-        step()
+    st = 0
+    for _ in range(warm):
+        decode_step(st)
+        st += 1
     torch.cuda.synchronize(device)
     assert cache.status() == 0
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    len0 = model.length()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     launches0 = kvq.kernel_launches()
-    with ClockSampler(device.index) as clk:
+    with ClockSampler(gpu_id(device)) as clk:
         barrier(device)
         torch.cuda.synchronize(device)
         t0.record(stream)
-        for i in range(args.steps):
-            step(evs[i])
+        for i in range(steps):
+            decode_step(st + i, evs[i])
         t1.record(stream)
         torch.cuda.synchronize(device)
         barrier(device)
     launches = kvq.kernel_launches() - launches0
     clocks = clk.summary()
     assert cache.status() == 0
+    st += steps
     total_ms = t0.elapsed_time(t1)
-    pre = [e[0].elapsed_time(e[1]) for e in evs]
-    app = [e[1].elapsed_time(e[2]) for e in evs]
-    dec = [e[2].elapsed_time(e[3]) for e in evs]
-
-    b_pre = A.prefill_bytes(wl, S)
-    b_app = A.append_bytes(wl, S)
-    b_dec = A.decode_bytes(wl, S + 1)
-    b_step = b_pre + b_app + b_dec
+    dec_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    app_ms = [e[2].elapsed_time(e[0]) for e in evs]
+    # decode bytes of each timed step (the cache grows by one token per step)
+    b_dec = [L * A.decode_bytes(wl, len0 + i + 1) for i in range(steps)]
+    all_dec_bytes = reduce_sum(sum(b_dec), device)
+    max_dec_ms = reduce_max(sum(dec_ms), device)
+    value = all_dec_bytes / (max_dec_ms * 1e-3) / 1e9
     max_ms = reduce_max(total_ms, device)
-    all_bytes = reduce_sum(b_step * args.steps, device)
-    value = all_bytes / (max_ms * 1e-3) / 1e9
     peak, peak_kind = hbm_peak()
-    m_pre, m_dec, m_app = statistics.mean(pre), statistics.mean(dec), statistics.mean(app)
+    launch_ms = sum(dec_ms) / (steps * L)  # average decode launch (one layer)
+    b_launch = sum(b_dec) / (steps * L)
 
-    # decode alone, L2 scrubbed before each launch (kernel timed in isolation)
-    scrub = torch.empty(512 << 20, dtype=torch.uint8, device=device)
-    alone = []
-    for i in range(max(5, args.steps)):
-        scrub.zero_()
+    # prefill quantize of layer 0 (K/V of the whole context), timed apart
+    qt = []
+    for i in range(3 + max(3, min(steps, 10))):
+        if flush is not None:
+            flush(i)
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        cache.decode(0, q, scale, out=out, workspace=ws)
+        cache.prefill(0, k0, v0)
         a1.record(stream)
         torch.cuda.synchronize(device)
-        alone.append(a0.elapsed_time(a1))
-    m_alone = statistics.median(alone)
-    del scrub
+        if i >= 3:
+            qt.append(a0.elapsed_time(a1))
+    b_pre = A.prefill_bytes(wl, model.S)
+    m_pre = statistics.median(qt)
+    # append of one token on layer 0 (restores the layer's length first)
+    del k0, v0
+    torch.cuda.synchronize(device)
 
-    e2e = run_e2e(args, wl, cache, k, v, q, k1, v1, out, ws, scale, device, b_step)
+    e2e = run_e2e(args, wl, model, st, device)
+    err = e2e_error(wl, model, device)
 
-    # dominant kernel of the step (by time): the quantize (prefill) step
-    dom = max((("prefill_quantize", m_pre, b_pre), ("decode_attention", m_dec, b_dec),
-               ("append_quantize", m_app, b_app)), key=lambda t: t[1])
-    gbs = lambda b, ms: b / (ms * 1e-3) / 1e9  # noqa: E731
-    traffic = load_traffic(wl, dom[0])
+    traffic = load_traffic(wl, "decode_attention")
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_ms / args.steps, 4),
+        "steps": steps, "warmup": warm, "ms_per_step": round(max_ms / steps, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded fp16, distribution of the workload)",
-        "config": {"workload": wl.name, "batch": wl.batch, "q_heads": wl.num_q_heads,
-                   "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "seq_len": S,
+        "config": {"workload": wl.name, "layers": L, "batch": wl.batch, "q_heads": wl.num_q_heads,
+                   "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "context": model.S,
                    "k_codec": codec_name(wl.k_bits, wl.k_mode, wl.k_group),
                    "v_codec": codec_name(wl.v_bits, wl.v_mode, wl.v_group),
                    "outliers_per_row": wl.outliers_per_row,
-                   "step": "prefill_quantize + append_quantize + decode_attention",
-                   "l2": "inputs larger than L2 (%.2f GiB fp16 K/V per step); decode_alone scrubs L2"
-                         % (2 * k.numel() * 2 / 2 ** 30)},
-        "decode_attention": {"gbs": round(gbs(b_dec, m_dec), 1), "ms": round(m_dec, 4),
-                             "bytes": b_dec, "frac": round(gbs(b_dec, m_dec) / peak, 4),
-                             "alone_l2_scrubbed_gbs": round(gbs(b_dec, m_alone), 1),
-                             "alone_frac": round(gbs(b_dec, m_alone) / peak, 4)},
+                   "step": "append_quantize on every layer, then decode_attention on every layer",
+                   "l2": ("flushed before each step (256 MB written then read); one layer's cache is %.0f MB"
+                          % (per_layer / 1e6)) if need_flush else
+                         ("inputs larger than L2: each layer's packed cache is %.0f MB and the %d layers are "
+                          "decoded in turn" % (per_layer / 1e6, L))},
+        "decode_attention": {"gbs": round(value, 1), "ms_per_step": round(max_dec_ms / steps, 4),
+                             "bytes_per_step": int(sum(b_dec) / steps),
+                             "frac": round(value / peak, 4),
+                             "launch_ms": round(launch_ms, 4), "launch_bytes": int(b_launch)},
+        "step_gbs": round(all_dec_bytes / (max_ms * 1e-3) / 1e9, 1),
         "quantize": {"gbs": round(gbs(b_pre, m_pre), 1), "ms": round(m_pre, 4), "bytes": b_pre,
-                     "frac": round(gbs(b_pre, m_pre) / peak, 4)},
-        "append_us": round(m_app * 1e3, 2),
-        "roofline": {"kernel": dom[0], "bound": "hbm", "achieved": round(gbs(dom[2], dom[1]), 1),
-                     "peak": peak, "peak_kind": peak_kind + " (hbm_gbs, copy)", "unit": "GB/s",
-                     "frac": round(gbs(dom[2], dom[1]) / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes": dom[2]},
+                     "frac": round(gbs(b_pre, m_pre) / peak, 4), "what": "prefill of one layer"},
+        "append_us_per_layer": round(statistics.mean(app_ms) / L * 1e3, 2),
+        "roofline": {"kernel": "decode_attention", "bound": "hbm",
+                     "achieved": round(gbs(b_launch, launch_ms), 1), "peak": peak,
+                     "peak_kind": peak_kind + " (hbm_gbs, copy; of measured)", "unit": "GB/s",
+                     "frac": round(gbs(b_launch, launch_ms) / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes": int(b_launch)},
+        "e2e_error": err,
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": launches,
     }
     return line
+
+
+def e2e_error(wl, model, device):
+    """Error of the decoded attention against fp64 attention on the
+    unquantized fp16 K/V (the inputs the cache was built from), for the
+    first stream of layer 0, by bit width. Reported, not gated."""
+    import numpy as np
+    from oracle import kvq_oracle as O
+    cache = model.cache
+    src = model.src[0]
+    n_len = model.length()
+    k, v = src.kv(model.S)
+    ks = [k[0, 0].cpu().numpy()]
+    vs = [v[0, 0].cpu().numpy()]
+    del k, v
+    for st in range(n_len - model.S):
+        _, k1, v1 = model.inputs[st][0]
+        ks.append(k1[0, 0:1].cpu().numpy())
+        vs.append(v1[0, 0:1].cpu().numpy())
+    kf = np.concatenate(ks, 0).astype(np.float64)[None]
+    vf = np.concatenate(vs, 0).astype(np.float64)[None]
+    q, _, _ = model.inputs[0][0]
+    qd = q.to(device)
+    o = cache.decode(0, qd, model.scale).cpu().double().numpy()[0, :wl.gqa][None]
+    ref = O.attend(q[0, :wl.gqa].cpu().double().numpy()[None], kf, vf, model.scale)
+    e = float(O.row_relative_error(o, ref).max())
+    return {"k%dv%d" % (wl.k_bits, wl.v_bits): round(e, 6),
+            "what": "max row error of layer 0, stream 0 (%d query heads, %d tokens) against fp64 attention "
+                    "on the unquantized fp16 K/V" % (wl.gqa, n_len)}
 
 
 def codec_name(bits, mode, group):
@@ -311,45 +424,43 @@ def load_traffic(wl, kernel):
     return None
 
 
-def run_e2e(args, wl, cache, k, v, q, k1, v1, out, ws, scale, device, b_step):
-    """The same step through host buffers: pinned host -> device copies of the
-    step's inputs, the three C-ABI calls, and a device -> host read of the
-    output, all inside the timed region."""
-    hk = torch.empty_like(k, device="cpu").pin_memory()
-    hv = torch.empty_like(v, device="cpu").pin_memory()
-    hq = torch.empty_like(q, device="cpu").pin_memory()
-    hk1 = torch.empty_like(k1, device="cpu").pin_memory()
-    hv1 = torch.empty_like(v1, device="cpu").pin_memory()
-    hout = torch.empty_like(out, device="cpu").pin_memory()
-    for h, d in ((hk, k), (hv, v), (hq, q), (hk1, k1), (hv1, v1)):
-        h.copy_(d)
-    dk, dv = torch.empty_like(k), torch.empty_like(v)
-    dq, dk1, dv1 = torch.empty_like(q), torch.empty_like(k1), torch.empty_like(v1)
-    h2d = sum(t.numel() * t.element_size() for t in (hk, hv, hq, hk1, hv1))
+def run_e2e(args, wl, model, st0, device):
+    """The same decode step through host buffers: pinned host -> device copies
+    of the step's q and appended K/V rows for every layer, the C-ABI calls,
+    and a device -> host read of every layer's output, all inside the timed
+    region."""
+    L = wl.num_layers
+    cache, ws, scale = model.cache, model.ws, model.scale
+    n = max(3, min(args.steps, 10))
+    host = []
+    for i in range(n + 1):
+        host.append([tuple(t.cpu().pin_memory() for t in model.inputs[st0 + i][l]) for l in range(L)])
+    dev = [tuple(torch.empty_like(t, device=device) for t in model.inputs[0][l]) for l in range(L)]
+    hout = torch.empty_like(model.out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0][0]) * L
     d2h = hout.numel() * hout.element_size()
 
-    def step():
-        dk.copy_(hk, non_blocking=True)
-        dv.copy_(hv, non_blocking=True)
-        dq.copy_(hq, non_blocking=True)
-        dk1.copy_(hk1, non_blocking=True)
-        dv1.copy_(hv1, non_blocking=True)
-        cache.prefill(0, dk, dv)
-        cache.append(0, dk1, dv1)
-        cache.decode(0, dq, scale, out=out, workspace=ws)
-        hout.copy_(out, non_blocking=True)
+    def step(i):
+        for l in range(L):
+            for d, h in zip(dev[l], host[i][l]):
+                d.copy_(h, non_blocking=True)
+        for l in range(L):
+            cache.append(l, dev[l][1], dev[l][2])
+        for l in range(L):
+            cache.decode(l, dev[l][0], scale, out=model.out[l], workspace=ws)
+        hout.copy_(model.out, non_blocking=True)
 
-    n = max(3, min(args.steps, 10))
-    for _ in range(2):
-        step()
+    step(0)
     torch.cuda.synchronize(device)
+    len0 = model.length()
     barrier(device)
     t = time.perf_counter()
-    for _ in range(n):
-        step()
+    for i in range(1, n + 1):
+        step(i)
     torch.cuda.synchronize(device)
     dt = reduce_max(time.perf_counter() - t, device)
-    tot = reduce_sum(b_step * n, device)
+    b = sum(L * A.decode_bytes(wl, len0 + i + 1) for i in range(n))
+    tot = reduce_sum(b, device)
     return {"value": round(tot / dt / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "ms_per_step": round(dt / n * 1e3, 3), "steps": n}
 
@@ -358,83 +469,80 @@ def run_e2e(args, wl, cache, k, v, q, k1, v1, out, ws, scale, device, b_step):
 # CPU oracle (the baseline and the reference arm)
 # ---------------------------------------------------------------------------
 
-def oracle_step_on_sample(wl, n_streams, seed):
-    """One full step of the oracle over the first n_streams (batch, kv-head)
-    streams of the workload; returns (seconds, algorithmic bytes)."""
-    import numpy as np
+def oracle_sample(wl, n_streams, seed):
+    """The oracle's cache for the first n_streams (batch, kv-head) streams of
+    layer 0 at the full context (prefill, untimed)."""
     from bit_quantized_kv_kvq_gb300.synth import LayerSource
     from oracle import kvq_oracle as O
-
     src = LayerSource(wl, 0, device="cpu", seed=seed)
     k, v = src.kv(wl.seq_len, batch=1)
-    q, k1, v1 = src.step(0, batch=1)
-    hk = k.shape[1]
-    n_streams = min(n_streams, hk)
-    kk = k[0, :n_streams].numpy()
-    vv = v[0, :n_streams].numpy()
-    g = wl.gqa
-    qq = q[0, :n_streams * g].double().numpy().reshape(n_streams, g, wl.head_dim)
+    n_streams = min(n_streams, wl.num_kv_heads)
     spec = O.CodecSpec(wl.head_dim, wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group,
                        wl.v_group, wl.outliers_per_row)
-    t = time.perf_counter()
     oc = O.OracleCache(spec, n_streams)
-    oc.prefill(kk, vv)
+    t = time.perf_counter()
+    oc.prefill(k[0, :n_streams].numpy(), v[0, :n_streams].numpy())
+    return oc, src, n_streams, time.perf_counter() - t
+
+
+def oracle_decode_step(wl, oc, src, n_streams, st):
+    """One decode step of the oracle on its sample: append one token per
+    stream, then decode attention; returns (seconds, decode bytes)."""
+    q, k1, v1 = src.step(st, batch=1)
+    g = wl.gqa
+    qq = q[0, :n_streams * g].double().numpy().reshape(n_streams, g, wl.head_dim)
+    t = time.perf_counter()
     oc.append(k1[0, :n_streams].numpy(), v1[0, :n_streams].numpy())
     oc.decode(qq, 1.0 / math.sqrt(wl.head_dim))
     dt = time.perf_counter() - t
     frac = n_streams / float(wl.batch * wl.num_kv_heads)
-    S = wl.seq_len
-    b = (A.prefill_bytes(wl, S) + A.append_bytes(wl, S) + A.decode_bytes(wl, S + 1)) * frac
-    del np
-    return dt, b
+    return dt, A.decode_bytes(wl, oc.length) * frac
 
 
 def cpu_sample(wl, budget_s):
-    """Times the oracle on a bounded sample of the workload: as many (batch,
-    kv-head) streams as one batch holds, repeated until about budget_s seconds
-    of CPU work have been spent."""
-    dt1, _ = oracle_step_on_sample(wl, 1, wl.seed)
-    n = max(1, min(wl.num_kv_heads, int(budget_s / max(dt1, 1e-3))))
-    tot_s, tot_b, reps = 0.0, 0.0, 0
-    while reps == 0 or tot_s < 0.8 * budget_s:
-        dt, b = oracle_step_on_sample(wl, n, wl.seed + reps)
+    """Times the oracle on a bounded sample: one (batch, kv-head) stream of
+    layer 0 at the full context, decode steps until about budget_s seconds
+    of CPU work; reports decode-attention GB/s scaled to the sample."""
+    oc, src, n, _ = oracle_sample(wl, 1, wl.seed)
+    tot_s, tot_b, st = 0.0, 0.0, 0
+    while st == 0 or tot_s < budget_s:
+        dt, b = oracle_decode_step(wl, oc, src, n, st)
         tot_s += dt
         tot_b += b
-        reps += 1
+        st += 1
     return {"value": round(tot_b / tot_s / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": "%d x %d of %d (batch, kv-head) streams at the full context %d, one full "
-                      "step each (prefill + append + decode), numpy single thread"
-                      % (reps, n, wl.batch * wl.num_kv_heads, wl.seq_len),
+            "sample": "%d decode steps (append + attention) of 1 of %d (batch, kv-head) streams of one "
+                      "layer at the full %d-token context, numpy single thread"
+                      % (st, wl.batch * wl.num_kv_heads, wl.seq_len),
             "seconds": round(tot_s, 2)}
 
 
 def run_reference(args, wl, rank, world):
     if rank != 0:
         return None
-    dt1, _ = oracle_step_on_sample(wl, 1, wl.seed)
-    budget_total = 150.0
-    per_step = budget_total / max(1, args.steps + args.warmup)
-    n = max(1, min(wl.num_kv_heads, int(per_step / max(dt1, 1e-3))))
-    for _ in range(args.warmup):
-        oracle_step_on_sample(wl, n, wl.seed)
+    oc, src, n, _ = oracle_sample(wl, 1, wl.seed)
+    for st in range(args.warmup):
+        oracle_decode_step(wl, oc, src, n, st)
     times, byts = [], []
-    for _ in range(args.steps):
-        dt, b = oracle_step_on_sample(wl, n, wl.seed)
+    for i in range(args.steps):
+        dt, b = oracle_decode_step(wl, oc, src, n, args.warmup + i)
         times.append(dt)
         byts.append(b)
     total = sum(times)
     value = sum(byts) / total / 1e9
-    sample = ("%d of %d (batch, kv-head) streams at the full context %d per step, numpy single "
-              "thread" % (n, wl.batch * wl.num_kv_heads, wl.seq_len))
+    sample = ("one decode step (append + attention) per step on 1 of %d (batch, kv-head) streams of "
+              "one layer at the full %d-token context, numpy single thread"
+              % (wl.batch * wl.num_kv_heads, wl.seq_len))
     return {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(total / args.steps * 1e3, 2), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded fp16, distribution of the workload)",
-        "config": {"workload": wl.name, "batch": wl.batch, "q_heads": wl.num_q_heads,
-                   "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "seq_len": wl.seq_len,
-                   "step": "prefill_quantize + append_quantize + decode_attention"},
+        "config": {"workload": wl.name, "layers": wl.num_layers, "batch": wl.batch,
+                   "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim,
+                   "context": wl.seq_len,
+                   "step": "append_quantize + decode_attention (oracle sample)"},
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -475,8 +583,8 @@ def profile_case(args, wl):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(W.BY_NAME))
     ap.add_argument("--cpu-budget", type=float, default=15.0)

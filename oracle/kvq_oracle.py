@@ -263,20 +263,49 @@ class CodecSpec:
     outliers_per_row: int = 0
 
 
-@dataclass
 class TensorState:
     """Quantized rows of one tensor (K or V) for N streams.
 
     codes: int64 [N][R][D]; scale16/zero16: float16 metadata, per token
     [N][R][D/G] or per channel block [N][R/T][D]; out_cols/out_vals:
     [N][R][k]; resid: float16 [N][r][D] keys awaiting a full block.
+
+    Rows arrive in pieces (a prefill, then one token per append); the pieces
+    are kept in lists and joined along the row axis when an array is read, so
+    that an append costs the size of its own rows (a data structure only:
+    the arrays read back are exactly the concatenation of what was added).
     """
-    codes: np.ndarray
-    scale16: np.ndarray
-    zero16: np.ndarray | None
-    out_cols: np.ndarray
-    out_vals: np.ndarray
-    resid: np.ndarray | None = None
+
+    _FIELDS = ("codes", "scale16", "zero16", "out_cols", "out_vals")
+
+    def __init__(self, codes, scale16, zero16, out_cols, out_vals, resid=None):
+        self._parts = {f: [] for f in self._FIELDS}
+        self._joined = {}
+        self._has_zero = zero16 is not None
+        self.add(codes=codes, scale16=scale16, zero16=zero16, out_cols=out_cols, out_vals=out_vals)
+        self.resid = resid
+
+    def add(self, **rows):
+        for f, a in rows.items():
+            if a is None:
+                continue
+            self._parts[f].append(np.asarray(a))
+            self._joined.pop(f, None)
+
+    def _get(self, f):
+        if f == "zero16" and not self._has_zero:
+            return None
+        if f not in self._joined:
+            parts = self._parts[f]
+            self._joined[f] = parts[0] if len(parts) == 1 else np.concatenate(parts, axis=1)
+            self._parts[f] = [self._joined[f]]
+        return self._joined[f]
+
+    codes = property(lambda self: self._get("codes"))
+    scale16 = property(lambda self: self._get("scale16"))
+    zero16 = property(lambda self: self._get("zero16"))
+    out_cols = property(lambda self: self._get("out_cols"))
+    out_vals = property(lambda self: self._get("out_vals"))
 
 
 def _quantize_rows_per_token(x16, bits, mode, group, k_out):
@@ -353,20 +382,11 @@ class OracleCache:
             if nfull:
                 c, s16, z16, cols, vals = _quantize_blocks_per_channel(
                     pend[:, :nfull], bits, group, ko)
-                st.codes = np.concatenate([st.codes, c], axis=1)
-                st.scale16 = np.concatenate([st.scale16, s16], axis=1)
-                st.zero16 = np.concatenate([st.zero16, z16], axis=1)
-                st.out_cols = np.concatenate([st.out_cols, cols], axis=1)
-                st.out_vals = np.concatenate([st.out_vals, vals], axis=1)
+                st.add(codes=c, scale16=s16, zero16=z16, out_cols=cols, out_vals=vals)
             st.resid = pend[:, nfull:].copy()
         else:
             c, s16, z16, cols, vals = _quantize_rows_per_token(x16, bits, mode, group, ko)
-            st.codes = np.concatenate([st.codes, c], axis=1)
-            st.scale16 = np.concatenate([st.scale16, s16], axis=1)
-            if z16 is not None:
-                st.zero16 = np.concatenate([st.zero16, z16], axis=1)
-            st.out_cols = np.concatenate([st.out_cols, cols], axis=1)
-            st.out_vals = np.concatenate([st.out_vals, vals], axis=1)
+            st.add(codes=c, scale16=s16, zero16=z16, out_cols=cols, out_vals=vals)
 
     # -- the decode-loop steps -------------------------------------------
     def prefill(self, k16, v16):
