@@ -31,6 +31,10 @@ kvq_status cuda_fail(cudaError_t e, const char* what) {
   return fail(KVQ_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Kernels launch on the current device, which must be the one that holds the
+// cache (a launch elsewhere would fault on the cache's addresses).
+kvq_status check_device(const kvq_cache* h);
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
@@ -160,9 +164,20 @@ struct kvq_cache {
   std::vector<int> len;
   int splits_override = 0;
   int sm_count = 0;
+  int device = 0;  // device that holds the buffer; launches need it current
 };
 
 namespace {
+
+kvq_status check_device(const kvq_cache* h) {
+  int dev = -1;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != h->device)
+    return fail(KVQ_ERR_INVALID_ARG, "the current device is %d but the cache lives on device %d", dev,
+                h->device);
+  return KVQ_OK;
+}
 
 kvq::TensorDev tensor_dev(const kvq_cache* h, int layer, bool is_k) {
   const kvq_config& c = h->cfg;
@@ -304,6 +319,7 @@ kvq_status kvq_cache_create(const kvq_config* cfg, void* dev_buf, size_t bytes, 
   h->bytes = bytes;
   h->len.assign(cfg->num_layers, 0);
   h->sm_count = sms > 0 ? sms : 1;
+  h->device = attr.device;
   *out = h;
   return KVQ_OK;
 }
@@ -316,6 +332,8 @@ kvq_status kvq_cache_destroy(kvq_cache* cache) {
 kvq_status kvq_prefill_quantize(kvq_cache* h, int32_t layer, const void* k, const void* v,
                                 int32_t seq_len, void* stream) {
   kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  s = check_device(h);
   if (s != KVQ_OK) return s;
   if (seq_len < 0) return fail(KVQ_ERR_INVALID_ARG, "seq_len must be >= 0");
   if (seq_len > h->cfg.max_seq)
@@ -338,6 +356,8 @@ kvq_status kvq_prefill_quantize(kvq_cache* h, int32_t layer, const void* k, cons
 kvq_status kvq_append_quantize(kvq_cache* h, int32_t layer, const void* k, const void* v,
                                void* stream) {
   kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  s = check_device(h);
   if (s != KVQ_OK) return s;
   if (!k || !v) return fail(KVQ_ERR_INVALID_ARG, "k and v must not be NULL");
   if (!aligned(k, 16) || !aligned(v, 16))
@@ -375,6 +395,8 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
                                 float softmax_scale, void* out, int32_t out_dtype,
                                 void* workspace, size_t ws_bytes, void* stream) {
   kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  s = check_device(h);
   if (s != KVQ_OK) return s;
   if (!q || !out || !workspace) return fail(KVQ_ERR_INVALID_ARG, "q, out and workspace must not be NULL");
   if (!aligned(q, 16) || !aligned(out, 16) || !aligned(workspace, 16))
@@ -493,6 +515,8 @@ kvq_status kvq_cache_length(const kvq_cache* h, int32_t layer, int32_t* len) {
 
 kvq_status kvq_cache_status(kvq_cache* h, void* stream, uint32_t* word) {
   if (!h) return fail(KVQ_ERR_INVALID_ARG, "cache handle is NULL");
+  const kvq_status ds = check_device(h);
+  if (ds != KVQ_OK) return ds;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
