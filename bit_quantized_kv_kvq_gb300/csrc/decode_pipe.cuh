@@ -67,7 +67,7 @@ struct Args {
   int length;           // tokens cached
   int kq;               // key rows held as codes (a multiple of T)
   int T;                // key block (tokens) = one chunk
-  int UT;               // tokens per unit (32)
+  int UT;               // tokens per unit (64: two subtiles of 32)
   int U;                // units per chunk
   int cps;              // chunks per stream
   long long n_chunks;   // chunks of all streams
@@ -297,9 +297,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto load_q = [&](int n) {
       const int b = n / Hkv, kvh = n - b * Hkv;
       __syncwarp();
-      for (int h = 0; h < H; ++h) {
-        const uint2 raw = *reinterpret_cast<const uint2*>(
-            a.q + ((int64_t)b * a.num_q_heads + kvh * H + h) * kHeadDim + 4 * lane);
+      uint2 rq[kHMax];  // every head's row in flight at once
+#pragma unroll
+      for (int h = 0; h < kHMax; ++h)
+        if (h < H)
+          rq[h] = __ldg(reinterpret_cast<const uint2*>(a.q + ((int64_t)b * a.num_q_heads + kvh * H + h) * kHeadDim +
+                                                        4 * lane));
+#pragma unroll
+      for (int h = 0; h < kHMax; ++h) {
+        if (h >= H) break;
+        const uint2 raw = rq[h];
         const float2 x01 = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
         const float2 x23 = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
         float v[4] = {x01.x * a.scale_log2, x01.y * a.scale_log2, x23.x * a.scale_log2,
@@ -478,12 +485,18 @@ __global__ void __launch_bounds__(kThreads, 1)
               P[i2][14] = cd & 0x00070007u;
               P[i2][15] = cd & 0x00380038u;
             }
+            // even and odd k-chunks in separate accumulators: four independent mma chains
+            float c2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
             for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
               for (int i2 = 0; i2 < 2; ++i2)
-                tc::mma(c[2 * np + i2], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3], P[i2][2 * kc],
-                        P[i2][2 * kc + 1]);
+                tc::mma((kc & 1) ? c2[i2] : c[2 * np + i2], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3],
+                        P[i2][2 * kc], P[i2][2 * kc + 1]);
+#pragma unroll
+            for (int i2 = 0; i2 < 2; ++i2)
+#pragma unroll
+              for (int e = 0; e < 4; ++e) c[2 * np + i2][e] += c2[i2][e];
           }
         }
       } else {
@@ -504,12 +517,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               kr[i2][4 * i + 3] = v.w;
             }
           }
+          float c2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
           for (int kc = 0; kc < 8; ++kc)
 #pragma unroll
             for (int i2 = 0; i2 < 2; ++i2)
-              tc::mma(c[2 * np + i2], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3], kr[i2][2 * kc],
-                      kr[i2][2 * kc + 1]);
+              tc::mma((kc & 1) ? c2[i2] : c[2 * np + i2], aq[kc][0], aq[kc][1], aq[kc][2], aq[kc][3],
+                      kr[i2][2 * kc], kr[i2][2 * kc + 1]);
+#pragma unroll
+          for (int i2 = 0; i2 < 2; ++i2)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[2 * np + i2][e] += c2[i2][e];
         }
       }
 
@@ -1014,11 +1032,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const unsigned char* st = ring + (size_t)s * a.stage_bytes;
           const int t0 = t0c + k * a.UT;
           if (k == 0) rebuild(rt, st + a.off_km);
-          if (t0 < a.length) {
-            const __half* kres = rt ? L.k.resid + (int64_t)n * L.k.resid_sstride + (int64_t)(t0 - a.kq) * kHeadDim
-                                    : nullptr;
-            subtile(st, 0, min(32, a.length - t0), rt, kres);
-          }
+          const __half* kres = rt ? L.k.resid + (int64_t)n * L.k.resid_sstride + (int64_t)(t0 - a.kq) * kHeadDim
+                                  : nullptr;
+#pragma unroll 1
+          for (int r0 = 0; r0 < a.UT && t0 + r0 < a.length; r0 += 32)
+            subtile(st, r0, min(32, a.length - t0 - r0), rt, kres);
           __syncwarp();
           if (lane == 0 && u + a.ns < n_units) {
             fence_proxy_async_smem();

@@ -55,7 +55,7 @@ template <int KB, int VB, int VG, bool OUTL>
 struct Plan {
   static constexpr int KROW = 4 * Pack<KB>::kWords, VROW = 4 * Pack<VB>::kWords;
   static constexpr int VGPR = kHeadDim / VG;
-  static constexpr int UT = 32;
+  static constexpr int UT = 64;  // tokens per unit: two subtiles of 32 per wait and refill
 
   // Fills the shared-memory layout of `a` (H, kout, T set) and returns the
   // dynamic shared memory the launch needs, or 0 if it does not fit.
