@@ -360,6 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           z2[s] = 0.0f;
         }
       }
+      // every query value first: the fragment stores below would otherwise
+      // order each head's loads after the previous head's stores
+      float qv[kHMax][4];
+#pragma unroll
+      for (int h = 0; h < kHMax; ++h)
+#pragma unroll
+        for (int s = 0; s < 4; ++s) qv[h][s] = h < H ? qn[h * kHeadDim + ch[s]] : 0.0f;
       float bias[kHMax];
 #pragma unroll
       for (int h = 0; h < kHMax; ++h) {
@@ -368,9 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           float v[4];
 #pragma unroll
           for (int s = 0; s < 4; ++s) {
-            const float qv = qn[h * kHeadDim + ch[s]];
-            v[s] = qv * s2[s];
-            bias[h] = fmaf(qv, z2[s], bias[h]);
+            v[s] = qv[h][s] * s2[s];
+            bias[h] = fmaf(qv[h][s], z2[s], bias[h]);
           }
           uint32_t lo01, lo23;
           const uint32_t hi01 = tc::split_pair(v[0], v[1], lo01);
@@ -922,6 +928,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g < H) {
           const float M = fmaxf(mA, m_run);
           const float al = ex2(mA - M), be = ex2(m_run - M);
+          // the accumulator's values first, so its loads are not ordered
+          // after the stores of earlier channels
+          float sv[NTV][2];
+#pragma unroll
+          for (int j = 0; j < NTV; ++j)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              int ch, sh, q;
+              vchan<VB, VG>(j, 2 * t4 + e, ch, sh, q);
+              sv[j][e] = ch < kHeadDim ? so[g * kHeadDim + ch] : 0.0f;
+            }
 #pragma unroll
           for (int j = 0; j < NTV; ++j)
 #pragma unroll
@@ -940,7 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // undo 2^-24 of the codes, 2^sh of the code position and 2^(6 - ev)
                 float o = fmaf(O[j][e] + O[j][e + 2], tc::exp2i(18 + eq - sh), zq);
                 if (OUTL) o += ocr[g * kHeadDim + ch];
-                so[g * kHeadDim + ch] = fmaf(al, so[g * kHeadDim + ch], be * o);
+                so[g * kHeadDim + ch] = fmaf(al, sv[j][e], be * o);
               }
             }
           if (t4 == 0) {
