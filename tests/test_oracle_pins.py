@@ -462,3 +462,137 @@ def test_zero_extremes_are_positive_zero():
     x = np.array([[-0.0, -0.0, -0.0, -0.0], [0.0, -0.0, 0.0, -0.0]], np.float16)
     _, s16, z16 = O.quantize_asym(x, 4)
     assert np.all(s16.view(np.uint16) == 0) and np.all(z16.view(np.uint16) == 0)
+
+
+# ---------------------------------------------------------------------------
+# Per-channel key blocks: each (block, channel) holds its own grid
+# ---------------------------------------------------------------------------
+
+def _channel_grid_keys(bits, block, nb, d, seed):
+    """Keys whose channel c in block b takes the grid values z_bc + k s_bc,
+    k = 0 .. 2^b - 1 (both ends present), in a token order that differs per
+    channel. s_bc and z_bc are integers times 2^-q_bc, with q_bc, s_bc and z_bc
+    different across blocks and channels, and every key is an integer below
+    2048 times a power of two, so it is exact in fp16."""
+    rng = np.random.default_rng(seed)
+    levels = 2 ** bits - 1
+    x = np.zeros((1, nb * block, d), np.float16)
+    s = np.zeros((nb, d))
+    z = np.zeros((nb, d))
+    k = np.zeros((nb, block, d), np.int64)
+    for b in range(nb):
+        for c in range(d):
+            q = 3 + (b + 2 * c) % 6
+            s_int = 1 + (3 * b + c) % 3
+            z_int = (c * 7 + b * 11) % (2047 - levels * s_int) - 300
+            s[b, c] = s_int * 2.0 ** -q
+            z[b, c] = z_int * 2.0 ** -q
+            ks = rng.integers(0, levels + 1, size=block)
+            ks[rng.permutation(block)[:2]] = [0, levels]  # both extremes somewhere
+            k[b, :, c] = ks
+            x[0, b * block:(b + 1) * block, c] = (z[b, c] + ks * s[b, c]).astype(np.float16)
+            assert np.array_equal(x[0, b * block:(b + 1) * block, c].astype(np.float64), z[b, c] + ks * s[b, c])
+    return x, s, z, k
+
+
+@pytest.mark.parametrize("bits", [3, 4, 8])
+def test_per_channel_blocks_recover_each_channels_grid(bits):
+    """[KVQuant] §2.2 item 1 and [W4A8-FA3] §2.4: a key group is one channel
+    over T consecutive tokens. With channel c of block b built on its own grid
+    z_bc + k s_bc, the block's metadata must be exactly (s_bc, z_bc) at
+    [stream][b][c] and the codes must be the grid indices k; grouping over
+    channels instead, or a transposed block, gives other extremes."""
+    block, nb, d = 64, 3, 128
+    x, s, z, k = _channel_grid_keys(bits, block, nb, d, seed=500 + bits)
+    spec = O.CodecSpec(d, bits, 8, O.ASYM_PER_CHANNEL, O.ASYM_PER_TOKEN, block, 64)
+    c = O.OracleCache(spec, 1)
+    c.prefill(x, x)
+    assert c.k.scale16.shape == (1, nb, d)
+    assert np.array_equal(c.k.scale16[0].astype(np.float64), s)
+    assert np.array_equal(c.k.zero16[0].astype(np.float64), z)
+    assert np.array_equal(c.k.codes[0], k.reshape(nb * block, d))
+    assert c.k.resid.shape[1] == 0
+
+
+def test_per_channel_perturbation_stays_in_its_block_and_channel():
+    """Raising one key of channel c in block b above the channel's maximum
+    changes that block-channel's scale and no other metadata or codes outside
+    it (the per-channel counterpart of group confinement, [TurboQuant-mem]
+    §2.3)."""
+    bits, block, nb, d = 4, 64, 3, 128
+    x, s, z, _ = _channel_grid_keys(bits, block, nb, d, seed=77)
+    spec = O.CodecSpec(d, bits, 8, O.ASYM_PER_CHANNEL, O.ASYM_PER_TOKEN, block, 64)
+    a = O.OracleCache(spec, 1)
+    a.prefill(x, x.copy())
+    bb, cc, tt = 1, 37, 5
+    y = x.copy()
+    y[0, bb * block + tt, cc] = np.float16(z[bb, cc] + 20 * s[bb, cc])
+    b = O.OracleCache(spec, 1)
+    b.prefill(y, x.copy())
+    ds = a.k.scale16 != b.k.scale16
+    assert ds[0, bb, cc] and ds.sum() == 1
+    assert np.array_equal(a.k.zero16, b.k.zero16)
+    dc = a.k.codes != b.k.codes
+    rows = np.nonzero(dc[0])[0]
+    assert set(np.nonzero(dc[0])[1]) == {cc}
+    assert rows.min() >= bb * block and rows.max() < (bb + 1) * block
+    assert np.array_equal(a.v.codes, b.v.codes)
+
+
+# ---------------------------------------------------------------------------
+# Footprint: CSR outliers and the fp16 key residual, by hand
+# ---------------------------------------------------------------------------
+
+def test_packed_bytes_csr_by_hand():
+    # dense-and-sparse 128K layer: 32 streams, 4-bit K per channel (T=64) and
+    # V per token (G=64), 2 outliers per row. Per stream and tensor: codes
+    # 131072 * 64 B, metadata 1 MiB, CSR 4 (131072 + 1) + 131072 * 2 * 4 B.
+    got = O.packed_cache_bytes(1, 1, 32, 128, 131072, 4, 4, O.ASYM_PER_CHANNEL,
+                               O.ASYM_PER_TOKEN, 64, 64, outliers_per_row=2)
+    per = 131072 * 64 + 2 ** 20 + 4 * 131073 + 131072 * 8
+    assert per == 11010052
+    assert got == 32 * 2 * per == 704643328
+
+
+def test_packed_bytes_key_residual_by_hand():
+    # S = 1000 with T = 64: 960 key rows as codes in 15 blocks, 40 fp16 keys.
+    got = O.packed_cache_bytes(1, 1, 1, 128, 1000, 4, 8, O.ASYM_PER_CHANNEL,
+                               O.ASYM_PER_TOKEN, 64, 64)
+    k = 960 * 64 + 15 * 128 * 4 + 40 * 128 * 2
+    v = 1000 * (128 + 2 * 4)
+    assert (k, v) == (79360, 136000)
+    assert got == k + v
+    # with 3 outliers per row: the key CSR covers the 960 coded rows only,
+    # the value CSR all 1000 rows
+    got = O.packed_cache_bytes(1, 1, 1, 128, 1000, 4, 8, O.ASYM_PER_CHANNEL,
+                               O.ASYM_PER_TOKEN, 64, 64, outliers_per_row=3)
+    assert got == k + v + (4 * 961 + 960 * 12) + (4 * 1001 + 1000 * 12)
+
+
+@pytest.mark.parametrize("length", [1, 63, 64, 1000, 4097])
+def test_bench_accounting_matches_oracle_footprint(length):
+    """bench.py's byte counts (the package's accounting module) equal the
+    oracle's footprint for every workload and ragged lengths."""
+    from bit_quantized_kv_kvq_gb300 import accounting as A, workloads as W
+    for wl in W.ALL:
+        want = O.packed_cache_bytes(1, wl.batch, wl.num_kv_heads, wl.head_dim, length, wl.k_bits,
+                                    wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group, wl.v_group,
+                                    wl.outliers_per_row)
+        assert A.cache_read_bytes(wl, length) == want, wl.name
+
+
+# ---------------------------------------------------------------------------
+# The error measure of the attention gate
+# ---------------------------------------------------------------------------
+
+def test_row_relative_error_closed_form():
+    """Reading R13: max_d |o - o_ref| / max_d |o_ref| per row."""
+    o_ref = np.array([[1.0, -4.0, 2.0], [-8.0, 1.0, 0.5], [0.0, 0.0, 0.0]])
+    o = np.array([[1.5, -4.0, 2.0], [-6.0, 1.0, 0.25], [0.0, 0.0, 0.0]])
+    got = O.row_relative_error(o, o_ref)
+    assert np.array_equal(got, [0.5 / 4.0, 2.0 / 8.0, 0.0])
+    # rows along the last axis only; the denominator is the reference's
+    assert O.row_relative_error(o_ref, o)[1] == 2.0 / 6.0
+    x = np.arange(24.0).reshape(2, 3, 4) + 1
+    e = O.row_relative_error(x * (1 + 1e-3), x)
+    assert e.shape == (2, 3) and np.allclose(e, 1e-3, rtol=1e-12)
