@@ -376,27 +376,27 @@ def run_gpu(args, wl, rank, world, device):
 def e2e_error(wl, model, device):
     """Error of the decoded attention against fp64 attention on the
     unquantized fp16 K/V (the inputs the cache was built from), for the
-    first stream of layer 0, by bit width. Reported, not gated."""
-    import numpy as np
-    from oracle import kvq_oracle as O
+    first stream of layer 0, by bit width: max over the stream's query heads
+    of max_d |o - o_ref| / max_d |o_ref|. The fp64 reference is plain torch
+    (softmax(q k^T scale) v) on the host. Reported, not gated."""
     cache = model.cache
     src = model.src[0]
     n_len = model.length()
     k, v = src.kv(model.S)
-    ks = [k[0, 0].cpu().numpy()]
-    vs = [v[0, 0].cpu().numpy()]
+    ks = [k[0, 0].cpu()]
+    vs = [v[0, 0].cpu()]
     del k, v
     for st in range(n_len - model.S):
         _, k1, v1 = model.inputs[st][0]
-        ks.append(k1[0, 0:1].cpu().numpy())
-        vs.append(v1[0, 0:1].cpu().numpy())
-    kf = np.concatenate(ks, 0).astype(np.float64)[None]
-    vf = np.concatenate(vs, 0).astype(np.float64)[None]
+        ks.append(k1[0, 0:1].cpu())
+        vs.append(v1[0, 0:1].cpu())
+    kf = torch.cat(ks, 0).double()
+    vf = torch.cat(vs, 0).double()
     q, _, _ = model.inputs[0][0]
-    qd = q.to(device)
-    o = cache.decode(0, qd, model.scale).cpu().double().numpy()[0, :wl.gqa][None]
-    ref = O.attend(q[0, :wl.gqa].cpu().double().numpy()[None], kf, vf, model.scale)
-    e = float(O.row_relative_error(o, ref).max())
+    o = cache.decode(0, q.to(device), model.scale).cpu().double()[0, :wl.gqa]
+    qf = q[0, :wl.gqa].cpu().double()
+    ref = torch.softmax((qf @ kf.T) * model.scale, dim=-1) @ vf
+    e = float(((o - ref).abs().amax(-1) / ref.abs().amax(-1).clamp_min(1e-30)).max())
     return {"k%dv%d" % (wl.k_bits, wl.v_bits): round(e, 6),
             "what": "max row error of layer 0, stream 0 (%d query heads, %d tokens) against fp64 attention "
                     "on the unquantized fp16 K/V" % (wl.gqa, n_len)}

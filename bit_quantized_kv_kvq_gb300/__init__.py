@@ -74,6 +74,9 @@ _SIGNATURES = {
     "kvq_cache_get_layout": [_P, _I, ctypes.POINTER(Layout)],
     "kvq_cache_length": [_P, _I, ctypes.POINTER(_I)],
     "kvq_cache_status": [_P, _P, ctypes.POINTER(ctypes.c_uint32)],
+    "kvq_selftest_div_levels": [_I, ctypes.c_uint32, ctypes.c_uint32, _P, _P],
+    "kvq_selftest_code_rounding": [_I, _I, _I, _I, _P, _P],
+    "kvq_selftest_wait_timeout": [_P, _I, _P],
 }
 
 _lib = None
@@ -99,6 +102,27 @@ def lib():
         L.kvq_kernel_launches.restype = ctypes.c_uint64
         _lib = L
     return _lib
+
+
+def _selftest_result(run, device):
+    res = torch.empty(2, dtype=torch.int64, device=device)
+    check(run(ctypes.c_void_p(res.data_ptr())))
+    mism, first = (int(x) & 0xFFFFFFFFFFFFFFFF for x in res.cpu().tolist())
+    return mism, first
+
+
+def selftest_div_levels(levels, a_first, a_last, device="cuda", stream=None):
+    """(mismatches, smallest mismatching fp32 bit pattern or 2^64 - 1) of the
+    prefill's scale division against IEEE division (kvq_selftest.h)."""
+    return _selftest_result(lambda r: lib().kvq_selftest_div_levels(levels, a_first, a_last, r,
+                                                                    _stream_ptr(stream)), device)
+
+
+def selftest_code_rounding(method, k_first, k_last, ulps, device="cuda", stream=None):
+    """(mismatches, smallest mismatching input key or 2^64 - 1) of the code
+    rounding near ties against IEEE division (kvq_selftest.h)."""
+    return _selftest_result(lambda r: lib().kvq_selftest_code_rounding(method, k_first, k_last, ulps, r,
+                                                                       _stream_ptr(stream)), device)
 
 
 def kernel_launches() -> int:
@@ -233,6 +257,10 @@ class QuantizedKVCache:
         w = ctypes.c_uint32()
         check(lib().kvq_cache_status(self.handle, _stream_ptr(stream), ctypes.byref(w)))
         return w.value
+
+    def selftest_wait_timeout(self, polls, stream=None):
+        """Runs the bounded-wait self-test on this cache (kvq_selftest.h)."""
+        check(lib().kvq_selftest_wait_timeout(self.handle, polls, _stream_ptr(stream)))
 
     def view(self, ptr, nbytes, dtype):
         """A tensor view of ``nbytes`` of the cache buffer starting at device

@@ -93,16 +93,21 @@ __device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parit
   return done != 0;
 }
 
-// Bounded wait: gives up after kWaitLimit suspended polls of at most
-// kWaitHintNs each (about a second in all) and reports false, so no thread
-// can wait forever.
+// Bounded wait: gives up after `polls` suspended polls of at most hint_ns
+// each and reports false, so no thread can wait forever.
+__device__ __forceinline__ bool mbar_wait_limited(uint64_t* bar, uint32_t parity, int polls,
+                                                  uint32_t hint_ns) {
+  for (int it = 0; it < polls; ++it) {
+    if (mbar_try_wait_hint(bar, parity, hint_ns)) return true;
+  }
+  return false;
+}
+
+// The kernels' wait: kWaitLimit polls of at most kWaitHintNs (about a second).
 constexpr int kWaitLimit = 1 << 17;
 constexpr uint32_t kWaitHintNs = 10000;
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (int it = 0; it < kWaitLimit; ++it) {
-    if (mbar_try_wait_hint(bar, parity, kWaitHintNs)) return true;
-  }
-  return false;
+  return mbar_wait_limited(bar, parity, kWaitLimit, kWaitHintNs);
 }
 
 // Orders this thread's earlier generic-proxy shared-memory accesses before

@@ -276,6 +276,10 @@ kvq_status check_layer(const kvq_cache* h, int layer) {
 namespace kvq {
 void set_error_message(const char* msg) { g_err = msg ? msg : ""; }
 
+uint32_t* cache_status_word(kvq_cache* h) { return reinterpret_cast<uint32_t*>(h->base); }
+
+kvq_status cache_device_is_current(const kvq_cache* h) { return check_device(h); }
+
 static std::atomic<uint64_t> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 }  // namespace kvq

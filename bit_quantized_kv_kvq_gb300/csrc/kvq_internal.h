@@ -97,6 +97,11 @@ cudaError_t launch_decode_gqa(const LayerDev& L, const DecodeArgs& a, cudaStream
 // Adds n to the process-wide count returned by kvq_kernel_launches().
 void count_launches(int n);
 
+// The device status word of a cache (its header), and the check that the
+// current device holds the cache (KVQ_ERR_INVALID_ARG, with a message, if not).
+uint32_t* cache_status_word(kvq_cache* h);
+kvq_status cache_device_is_current(const kvq_cache* h);
+
 // Replaces the thread-local message returned by kvq_last_error().
 void set_error_message(const char* msg);
 

@@ -22,13 +22,14 @@ def lib():
 
 
 def declared_entry_points():
-    src = open(os.path.join(ROOT, "include", "kvq.h")).read()
+    inc = os.path.join(ROOT, "include")
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     return sorted(set(re.findall(r"KVQ_API\s+[\w\s\*]+?\b(kvq_\w+)\s*\(", src)))
 
 
 def test_every_declared_symbol_is_exported(lib):
     names = declared_entry_points()
-    assert len(names) >= 13
+    assert len(names) >= 16 and "kvq_selftest_wait_timeout" in names
     for n in names:
         assert hasattr(lib, n), n
 
