@@ -156,10 +156,10 @@ cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t s
     combine = false;  // one split writes the output itself; the last CTA of a stream merges the splits
   } else if (a.gqa == 1 && decode_mha_supported(L)) {
     e = launch_decode_mha(L, a, st);
-    combine = a.splits > 1;  // one split writes the output itself
+    combine = false;  // as above
   } else if (a.gqa > 1 && decode_gqa_supported(L, a.gqa)) {
     e = launch_decode_gqa(L, a, st);
-    combine = a.splits > 1;
+    combine = false;  // as above
   } else {
     switch (a.gqa) {
       case 1: e = launch_decode_g1(L, a, st); break;

@@ -20,6 +20,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "decode_merge.cuh"
 
 namespace kvq {
 namespace gqa {
@@ -668,6 +669,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
     }
   }
+  if (a.splits > 1) merge_splits_if_last<kWarps>(L.counters + n, a, b * a.num_q_heads + hq0, G);
 }
 
 template <int KB, int KMODE, int VB, int VMODE>

@@ -18,6 +18,7 @@
 #pragma once
 
 #include "common.cuh"
+#include "decode_merge.cuh"
 
 namespace kvq {
 namespace mha {
@@ -473,6 +474,7 @@ __global__ void __launch_bounds__(kThreads, 4)
       a.part_ml[r * 2 + 1] = lsum;
     }
   }
+  if (a.splits > 1) merge_splits_if_last<kWarps>(L.counters + n, a, (int64_t)b * a.num_q_heads + hq, 1);
 }
 
 template <int KB, int KMODE, int VB, int VMODE, bool OUTL>

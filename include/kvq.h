@@ -237,8 +237,12 @@ KVQ_API const char* kvq_last_error(void);
 
 /* Number of device kernels this process has enqueued through the library
  * (all caches, all threads), counted on the host at each successful
- * launch: prefill 1, append 1, decode 1 plus 1 for the split combine when
- * the work was split. Occupancy queries launch nothing and are not counted. */
+ * launch: prefill 1, append 1, decode 1 (the split partials are merged by
+ * the last CTA of each stream inside the decode kernel), except the generic
+ * decode used for the rarer codec combinations (per-token keys with
+ * outliers, sub-32-channel groups), which adds 1 for a combine launch;
+ * each self-test call 1. Occupancy queries launch
+ * nothing and are not counted. */
 KVQ_API uint64_t kvq_kernel_launches(void);
 
 /* Library version, major * 10000 + minor * 100 + patch. */

@@ -172,12 +172,17 @@ def test_errors_are_reported_not_raised_on_device():
 
 def test_launch_counter_matches_the_work_enqueued():
     """prefill, append and decode enqueue one kernel each. The stream-K decode
-    (per-channel keys, 8 query heads per kv-head) merges its splits inside its
-    one kernel; the split-K decodes add the split combine when split."""
+    (per-channel keys, 8 query heads per kv-head) and the split decodes of the
+    common codecs merge their splits inside their one kernel; only the
+    generic decode adds a combine launch (also with one split)."""
     import bit_quantized_kv_kvq_gb300 as kvq
-    for kmode, hq, extra_split in ((W.ASYM_PER_CHANNEL, 32, 1), (W.ASYM_PER_TOKEN, 4, 2)):
+    cases = ((W.ASYM_PER_CHANNEL, 32, 0, 1, 1),  # stream-K
+             (W.ASYM_PER_CHANNEL, 16, 0, 1, 1),  # token-row tensor-core split decode
+             (W.ASYM_PER_TOKEN, 4, 0, 1, 1),     # one query head per kv-head
+             (W.ASYM_PER_TOKEN, 8, 2, 2, 2))     # outliers with per-token keys: generic kernel + combine
+    for kmode, hq, outl, extra_one, extra_split in cases:
         wl = replace(W.LLAMA7B_16K, batch=1, num_q_heads=hq, num_kv_heads=4, seq_len=300, k_mode=kmode,
-                     k_group=64 if kmode == W.ASYM_PER_CHANNEL else 32)
+                     k_group=64 if kmode == W.ASYM_PER_CHANNEL else 32, outliers_per_row=outl)
         src = LayerSource(wl, 0, device="cpu")
         k, v = src.kv(wl.seq_len)
         q, k1, v1 = src.step(0)
@@ -186,7 +191,7 @@ def test_launch_counter_matches_the_work_enqueued():
         cache.prefill(0, k.cuda(), v.cuda())
         cache.append(0, k1.cuda(), v1.cuda())
         assert kvq.kernel_launches() - n0 == 2
-        for splits, extra in ((1, 1), (3, extra_split)):
+        for splits, extra in ((1, extra_one), (3, extra_split)):
             cache.set_decode_splits(splits)
             n1 = kvq.kernel_launches()
             cache.decode(0, q.cuda(), 0.1)
