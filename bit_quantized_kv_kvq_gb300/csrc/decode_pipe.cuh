@@ -38,6 +38,7 @@
 #include <cuda.h>
 
 #include "mma_frag.cuh"
+#include "tensor_map.cuh"
 
 namespace kvq {
 namespace pipe {
@@ -82,20 +83,6 @@ struct Args {
   int w_qn, w_frag, w_eq, w_kz, w_ocr;  // offsets inside a consumer warp's scratch
 };
 
-// 2-D/3-D tensor copy of a box of code rows into shared memory.
-__device__ __forceinline__ void tma_rows(void* dst, const CUtensorMap* map, int row, int stream,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(row), "r"(stream), "r"(smem_u32(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void prefetch_map(const CUtensorMap* map) {
-  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
@@ -108,13 +95,6 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return __byte_perm(a, b, sel);
-}
-
-// Byte offset of a (row, byte) position inside a tile copied with the 64- or
-// 128-byte bank swizzle (16-byte chunk index XOR address bits 7..9).
-template <int RB>
-__device__ __forceinline__ uint32_t swz(uint32_t off) {
-  return off ^ (((off >> 7) & (RB == 128 ? 7u : 3u)) << 4);
 }
 
 __device__ __forceinline__ uint32_t u4(const uint4& v, int i) {

@@ -4,10 +4,7 @@
 // KVQ_PIPE_VB.
 #pragma once
 
-#include <cudaTypedefs.h>
-
 #include <cstring>
-#include <mutex>
 
 #include "decode_pipe.cuh"
 
@@ -15,39 +12,6 @@ namespace kvq {
 namespace pipe {
 
 inline int round_up_i(int x, int m) { return (x + m - 1) / m * m; }
-
-// cuTensorMapEncodeTiled from the driver, looked up once.
-inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult qr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &qr) ==
-            cudaSuccess &&
-        qr == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// Code rows of one tensor as a uint8 tensor [stream][row][byte]; a box is
-// `box_rows` whole rows, written to shared memory with the bank swizzle of the
-// row width (64 or 128 bytes).
-inline cudaError_t encode_rows(CUtensorMap* m, const void* base, int row_bytes, int cap, int n_streams,
-                               int64_t stream_bytes, int box_rows) {
-  PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
-  if (!fn) return cudaErrorNotSupported;
-  const cuuint64_t dims[3] = {(cuuint64_t)row_bytes, (cuuint64_t)cap, (cuuint64_t)n_streams};
-  const cuuint64_t strides[2] = {(cuuint64_t)row_bytes, (cuuint64_t)stream_bytes};
-  const cuuint32_t box[3] = {(cuuint32_t)row_bytes, (cuuint32_t)box_rows, 1u};
-  const cuuint32_t es[3] = {1u, 1u, 1u};
-  const CUtensorMapSwizzle sw = row_bytes == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
-}
 
 constexpr int kSmemMax = 232448;  // dynamic shared memory per CTA on sm_103a (227 KB)
 
