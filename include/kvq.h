@@ -33,6 +33,9 @@
  *  - fp16 means IEEE binary16. Layouts are C order (last index fastest).
  *  - One cache serves num_layers layers; lengths are uniform over the
  *    batch. head_dim must be 128.
+ *  - Calls that enqueue work (prefill, append, decode, status) need the
+ *    device that holds the cache buffer to be current; otherwise they
+ *    return KVQ_ERR_INVALID_ARG.
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -177,7 +180,7 @@ KVQ_API kvq_status kvq_append_quantize(kvq_cache* cache, int32_t layer, const vo
                                const void* v, void* stream);
 
 /* Workspace bytes kvq_decode_attention needs for `num_q_heads` query heads
- * at any length up to max_seq (split partials and counters). Host only. */
+ * at any length up to max_seq (the split partials). Host only. */
 KVQ_API kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_q_heads,
                                       size_t* bytes);
 
@@ -189,6 +192,15 @@ KVQ_API kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t nu
  * h reads KV head h / (H_q / H_kv); H_q must be a multiple of H_kv with
  * H_q / H_kv in {1, 2, 4, 8}. workspace: device scratch of at least
  * kvq_decode_workspace_bytes bytes, not shared with concurrent calls.
+ * Splits of the sequence are merged (log-sum-exp) inside the decode kernel by
+ * the last CTA of each stream, which counts arrivals on per-layer counters
+ * held in the cache buffer; every call leaves them at zero. Decode calls on
+ * the same layer therefore must not overlap on the GPU (one stream per layer,
+ * or ordered streams); calls on different layers may.
+ * With 8 query heads per kv-head (per-channel keys, per-token values) the
+ * decode is one persistent launch over all streams (stream-K: the key blocks
+ * of all streams cut into one range per SM), otherwise one CTA per (split,
+ * stream).
  * Errors: KVQ_ERR_INVALID_ARG when the layer is empty;
  * KVQ_ERR_BUFFER_TOO_SMALL for a short workspace. */
 KVQ_API kvq_status kvq_decode_attention(kvq_cache* cache, int32_t layer, const void* q,
@@ -216,8 +228,10 @@ KVQ_API kvq_status kvq_decode_attention_static(kvq_cache* cache, int32_t layer, 
                                                int32_t num_q_heads, float softmax_scale,
                                                void* out, int32_t out_dtype, void* stream);
 
-/* Forces the number of sequence splits of later decode calls (0 = automatic).
- * Results agree for every split count up to rounding; used by tests. */
+/* Forces the number of sequence splits of later decode calls (0 = automatic):
+ * for the stream-K decode the number of persistent CTAs (at most one per SM),
+ * otherwise the splits per stream. Results agree for every count up to
+ * rounding; used by tests. */
 KVQ_API kvq_status kvq_cache_set_decode_splits(kvq_cache* cache, int32_t splits);
 
 /* Layout and device pointers of layer `layer` (host only, no sync). */
@@ -229,7 +243,8 @@ KVQ_API kvq_status kvq_cache_length(const kvq_cache* cache, int32_t layer, int32
 /* Synchronizes `stream`, reads the device status word and clears it.
  * Returns KVQ_OK, KVQ_ERR_TIMEOUT (a bounded device wait gave up) or
  * KVQ_ERR_DEVICE_STATUS (a device-side check failed); *word (optional)
- * receives the raw bits. */
+ * receives the raw bits. After a nonzero word the split-merge counters of
+ * every layer are cleared too (a decode that gave up may have left them set). */
 KVQ_API kvq_status kvq_cache_status(kvq_cache* cache, void* stream, uint32_t* word);
 
 /* Thread-local description of the last error ("" if none). */
