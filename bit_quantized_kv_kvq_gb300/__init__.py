@@ -64,6 +64,9 @@ _I = ctypes.c_int32
 _SIGNATURES = {
     "kvq_cache_bytes": [ctypes.POINTER(Config), ctypes.POINTER(ctypes.c_size_t)],
     "kvq_cache_create": [ctypes.POINTER(Config), _P, ctypes.c_size_t, _P, ctypes.POINTER(_P)],
+    "kvq_cache_bytes_per_layer": [ctypes.POINTER(Config), ctypes.POINTER(_I), ctypes.POINTER(ctypes.c_size_t)],
+    "kvq_cache_create_per_layer": [ctypes.POINTER(Config), ctypes.POINTER(_I), _P, ctypes.c_size_t, _P,
+                                   ctypes.POINTER(_P)],
     "kvq_cache_destroy": [_P],
     "kvq_prefill_quantize": [_P, _I, _P, _P, _I, _P],
     "kvq_append_quantize": [_P, _I, _P, _P, _P],
@@ -168,15 +171,27 @@ class QuantizedKVCache:
 
     def __init__(self, num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits,
                  k_mode, v_mode, k_group, v_group, outliers_per_row=0, device=None,
-                 stream=None):
+                 stream=None, layer_bits=None):
+        """layer_bits: None, or one (k_bits, v_bits) pair per layer overriding
+        k_bits / v_bits (kvq_cache_create_per_layer)."""
         self.cfg = make_config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits,
                                v_bits, k_mode, v_mode, k_group, v_group, outliers_per_row)
-        self.nbytes = cache_bytes(self.cfg)
+        self.layer_bits = None
+        lb = None
+        if layer_bits is not None:
+            pairs = [tuple(int(b) for b in p) for p in layer_bits]
+            if len(pairs) != num_layers or any(len(p) != 2 for p in pairs):
+                raise ValueError("layer_bits needs one (k_bits, v_bits) pair per layer")
+            self.layer_bits = pairs
+            lb = (_I * (2 * num_layers))(*[b for p in pairs for b in p])
+        n = ctypes.c_size_t()
+        check(lib().kvq_cache_bytes_per_layer(ctypes.byref(self.cfg), lb, ctypes.byref(n)))
+        self.nbytes = n.value
         self.device = torch.device(device if device is not None else "cuda")
         self.buffer = torch.empty(self.nbytes, dtype=torch.uint8, device=self.device)
         h = ctypes.c_void_p()
-        check(lib().kvq_cache_create(ctypes.byref(self.cfg), ctypes.c_void_p(self.buffer.data_ptr()),
-                                     self.nbytes, _stream_ptr(stream), ctypes.byref(h)))
+        check(lib().kvq_cache_create_per_layer(ctypes.byref(self.cfg), lb, ctypes.c_void_p(self.buffer.data_ptr()),
+                                               self.nbytes, _stream_ptr(stream), ctypes.byref(h)))
         self.handle = h
         self._ws = {}
 

@@ -58,12 +58,18 @@ struct TensorPlan {
   int words = 0;
 };
 
+// One layer: its code widths and tensors, offsets relative to the layer base.
+struct LayerPlan {
+  int k_bits = 0, v_bits = 0;
+  TensorPlan k, v;
+  int64_t ctr_off = 0;  // uint32 split-merge counters [n_streams]
+  int64_t base = 0;     // from the start of the buffer
+};
+
 struct Plan {
   int capacity = 0;
   int64_t n_streams = 0;
-  TensorPlan k, v;
-  int64_t ctr_off = 0;  // per layer: uint32 split-merge counters [n_streams]
-  int64_t layer_bytes = 0;
+  std::vector<LayerPlan> layer;
   int64_t header_bytes = 256;
   int64_t total = 0;
 };
@@ -94,7 +100,7 @@ kvq_status check_tensor(const char* name, int bits, int mode, int group, bool is
   return KVQ_OK;
 }
 
-kvq_status check_config(const kvq_config* c) {
+kvq_status check_config(const kvq_config* c, const int32_t* layer_bits = nullptr) {
   if (!c) return fail(KVQ_ERR_INVALID_ARG, "config is NULL");
   if (c->num_layers < 1 || c->batch < 1 || c->num_kv_heads < 1 || c->max_seq < 1)
     return fail(KVQ_ERR_INVALID_ARG, "num_layers, batch, num_kv_heads and max_seq must be >= 1");
@@ -108,11 +114,20 @@ kvq_status check_config(const kvq_config* c) {
     return fail(KVQ_ERR_INVALID_ARG, "outliers_per_row must be in [0, %d]", kvq::kMaxOutliers);
   kvq_status s = check_tensor("k", c->k_bits, c->k_mode, c->k_group, true);
   if (s != KVQ_OK) return s;
-  return check_tensor("v", c->v_bits, c->v_mode, c->v_group, false);
+  s = check_tensor("v", c->v_bits, c->v_mode, c->v_group, false);
+  if (s != KVQ_OK || !layer_bits) return s;
+  for (int l = 0; l < c->num_layers; ++l) {
+    s = check_tensor("layer k", layer_bits[2 * l], c->k_mode, c->k_group, true);
+    if (s == KVQ_OK) s = check_tensor("layer v", layer_bits[2 * l + 1], c->v_mode, c->v_group, false);
+    if (s != KVQ_OK) {
+      const std::string m = kvq_last_error();
+      return fail(s, "layer %d: %s", l, m.c_str());
+    }
+  }
+  return KVQ_OK;
 }
 
-void plan_tensor(const kvq_config& c, int cap, bool is_k, int64_t* cursor, TensorPlan* t) {
-  const int bits = is_k ? c.k_bits : c.v_bits;
+void plan_tensor(const kvq_config& c, int bits, int cap, bool is_k, int64_t* cursor, TensorPlan* t) {
   const int mode = is_k ? c.k_mode : c.v_mode;
   const int group = is_k ? c.k_group : c.v_group;
   const int64_t n = (int64_t)c.batch * c.num_kv_heads;
@@ -138,19 +153,28 @@ void plan_tensor(const kvq_config& c, int cap, bool is_k, int64_t* cursor, Tenso
   }
 }
 
-Plan make_plan(const kvq_config& c) {
+// layer_bits: NULL (every layer takes c.k_bits / c.v_bits) or [num_layers][2].
+Plan make_plan(const kvq_config& c, const int32_t* layer_bits = nullptr) {
   Plan p;
   int64_t gran = kvq::kTile;
   if (c.k_mode == KVQ_ASYM_PER_CHANNEL && c.k_group > gran) gran = c.k_group;
   p.capacity = (int)round_up(c.max_seq, gran);
   p.n_streams = (int64_t)c.batch * c.num_kv_heads;
-  int64_t cursor = 0;
-  plan_tensor(c, p.capacity, true, &cursor, &p.k);
-  plan_tensor(c, p.capacity, false, &cursor, &p.v);
-  p.ctr_off = cursor;
-  cursor = round_up(cursor + p.n_streams * 4, 256);
-  p.layer_bytes = cursor;
-  p.total = p.header_bytes + p.layer_bytes * c.num_layers;
+  p.layer.resize(c.num_layers);
+  int64_t base = p.header_bytes;
+  for (int l = 0; l < c.num_layers; ++l) {
+    LayerPlan& lp = p.layer[l];
+    lp.k_bits = layer_bits ? layer_bits[2 * l] : c.k_bits;
+    lp.v_bits = layer_bits ? layer_bits[2 * l + 1] : c.v_bits;
+    int64_t cursor = 0;
+    plan_tensor(c, lp.k_bits, p.capacity, true, &cursor, &lp.k);
+    plan_tensor(c, lp.v_bits, p.capacity, false, &cursor, &lp.v);
+    lp.ctr_off = cursor;
+    cursor = round_up(cursor + p.n_streams * 4, 256);
+    lp.base = base;
+    base += cursor;
+  }
+  p.total = base;
   return p;
 }
 
@@ -181,10 +205,11 @@ kvq_status check_device(const kvq_cache* h) {
 
 kvq::TensorDev tensor_dev(const kvq_cache* h, int layer, bool is_k) {
   const kvq_config& c = h->cfg;
-  const TensorPlan& t = is_k ? h->plan.k : h->plan.v;
-  unsigned char* lb = h->base + h->plan.header_bytes + (int64_t)layer * h->plan.layer_bytes;
+  const LayerPlan& lp = h->plan.layer[layer];
+  const TensorPlan& t = is_k ? lp.k : lp.v;
+  unsigned char* lb = h->base + lp.base;
   kvq::TensorDev d;
-  d.bits = is_k ? c.k_bits : c.v_bits;
+  d.bits = is_k ? lp.k_bits : lp.v_bits;
   d.mode = is_k ? c.k_mode : c.v_mode;
   d.group = is_k ? c.k_group : c.v_group;
   d.words = t.words;
@@ -213,8 +238,7 @@ kvq::LayerDev layer_dev(const kvq_cache* h, int layer) {
   L.capacity = h->plan.capacity;
   L.outliers = h->cfg.outliers_per_row;
   L.status = reinterpret_cast<uint32_t*>(h->base);
-  L.counters = reinterpret_cast<uint32_t*>(h->base + h->plan.header_bytes +
-                                           (int64_t)layer * h->plan.layer_bytes + h->plan.ctr_off);
+  L.counters = reinterpret_cast<uint32_t*>(h->base + h->plan.layer[layer].base + h->plan.layer[layer].ctr_off);
   return L;
 }
 
@@ -286,23 +310,27 @@ void count_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order
 
 extern "C" {
 
-kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes) {
+kvq_status kvq_cache_bytes_per_layer(const kvq_config* cfg, const int32_t* layer_bits, size_t* bytes) {
   if (!bytes) return fail(KVQ_ERR_INVALID_ARG, "bytes is NULL");
-  kvq_status s = check_config(cfg);
+  kvq_status s = check_config(cfg, layer_bits);
   if (s != KVQ_OK) return s;
-  *bytes = (size_t)make_plan(*cfg).total;
+  *bytes = (size_t)make_plan(*cfg, layer_bits).total;
   return KVQ_OK;
 }
 
-kvq_status kvq_cache_create(const kvq_config* cfg, void* dev_buf, size_t bytes, void* stream,
-                            kvq_cache** out) {
+kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes) {
+  return kvq_cache_bytes_per_layer(cfg, nullptr, bytes);
+}
+
+kvq_status kvq_cache_create_per_layer(const kvq_config* cfg, const int32_t* layer_bits, void* dev_buf,
+                                      size_t bytes, void* stream, kvq_cache** out) {
   if (!out) return fail(KVQ_ERR_INVALID_ARG, "out is NULL");
   *out = nullptr;
-  kvq_status s = check_config(cfg);
+  kvq_status s = check_config(cfg, layer_bits);
   if (s != KVQ_OK) return s;
   if (!dev_buf) return fail(KVQ_ERR_INVALID_ARG, "dev_buf is NULL");
   if (!aligned(dev_buf, 256)) return fail(KVQ_ERR_INVALID_ARG, "dev_buf must be 256-byte aligned");
-  Plan p = make_plan(*cfg);
+  Plan p = make_plan(*cfg, layer_bits);
   if ((int64_t)bytes < p.total)
     return fail(KVQ_ERR_BUFFER_TOO_SMALL, "cache buffer has %zu bytes, needs %lld", bytes,
                 (long long)p.total);
@@ -326,6 +354,11 @@ kvq_status kvq_cache_create(const kvq_config* cfg, void* dev_buf, size_t bytes, 
   h->device = attr.device;
   *out = h;
   return KVQ_OK;
+}
+
+kvq_status kvq_cache_create(const kvq_config* cfg, void* dev_buf, size_t bytes, void* stream,
+                            kvq_cache** out) {
+  return kvq_cache_create_per_layer(cfg, nullptr, dev_buf, bytes, stream, out);
 }
 
 kvq_status kvq_cache_destroy(kvq_cache* cache) {
@@ -383,15 +416,24 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* h, int32_t num_q_heads, s
   if (!h || !bytes) return fail(KVQ_ERR_INVALID_ARG, "NULL argument");
   if (num_q_heads < 1) return fail(KVQ_ERR_INVALID_ARG, "num_q_heads must be >= 1");
   const int hkv = h->cfg.num_kv_heads;
-  if (num_q_heads % hkv == 0) {
-    kvq::LayerDev L = layer_dev(h, 0);
-    if (kvq::decode_pipe_supported(L, num_q_heads / hkv)) {
-      *bytes = kvq::decode_pipe_workspace_max(L, num_q_heads / hkv, h->sm_count);
-      return KVQ_OK;
+  // the largest need over the layers (their code widths may differ)
+  size_t need = 0;
+  bool split = false;
+  for (int l = 0; l < h->cfg.num_layers; ++l) {
+    kvq::LayerDev L = layer_dev(h, l);
+    if (num_q_heads % hkv == 0 && kvq::decode_pipe_supported(L, num_q_heads / hkv)) {
+      const size_t b = kvq::decode_pipe_workspace_max(L, num_q_heads / hkv, h->sm_count);
+      if (b > need) need = b;
+    } else {
+      split = true;
     }
   }
-  const int max_splits = h->plan.capacity / kvq::kTile;  // one tile per split at most
-  *bytes = workspace_for(h, num_q_heads, max_splits);
+  if (split) {
+    const int max_splits = h->plan.capacity / kvq::kTile;  // one tile per split at most
+    const size_t b = workspace_for(h, num_q_heads, max_splits);
+    if (b > need) need = b;
+  }
+  *bytes = need;
   return KVQ_OK;
 }
 
@@ -483,18 +525,19 @@ kvq_status kvq_cache_get_layout(const kvq_cache* h, int32_t layer, kvq_layout* o
   o->length = len;
   o->k_quantized_len = k_quant_len(h->cfg, len);
   o->k_resid_len = len - o->k_quantized_len;
-  o->k_words_per_row = h->plan.k.words;
-  o->v_words_per_row = h->plan.v.words;
-  o->k_meta_entry_bytes = h->plan.k.meta_bytes;
-  o->v_meta_entry_bytes = h->plan.v.meta_bytes;
-  o->k_codes_stream_bytes = h->plan.k.codes_sb;
-  o->v_codes_stream_bytes = h->plan.v.codes_sb;
-  o->k_meta_stream_bytes = h->plan.k.meta_sb;
-  o->v_meta_stream_bytes = h->plan.v.meta_sb;
-  o->k_resid_stream_bytes = h->plan.k.resid_sb;
-  o->out_rowptr_stream_bytes = h->plan.k.rp_sb;
-  o->out_col_stream_bytes = h->plan.k.col_sb;
-  o->out_val_stream_bytes = h->plan.k.val_sb;
+  const LayerPlan& lp = h->plan.layer[layer];
+  o->k_words_per_row = lp.k.words;
+  o->v_words_per_row = lp.v.words;
+  o->k_meta_entry_bytes = lp.k.meta_bytes;
+  o->v_meta_entry_bytes = lp.v.meta_bytes;
+  o->k_codes_stream_bytes = lp.k.codes_sb;
+  o->v_codes_stream_bytes = lp.v.codes_sb;
+  o->k_meta_stream_bytes = lp.k.meta_sb;
+  o->v_meta_stream_bytes = lp.v.meta_sb;
+  o->k_resid_stream_bytes = lp.k.resid_sb;
+  o->out_rowptr_stream_bytes = lp.k.rp_sb;
+  o->out_col_stream_bytes = lp.k.col_sb;
+  o->out_val_stream_bytes = lp.k.val_sb;
   o->k_codes = L.k.codes;
   o->k_meta = L.k.meta;
   o->k_resid = L.k.resid;
@@ -532,7 +575,7 @@ kvq_status kvq_cache_status(kvq_cache* h, void* stream, uint32_t* word) {
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemset status");
     // a decode that gave up may have left split-merge counters set
     for (int l = 0; l < h->cfg.num_layers; ++l) {
-      e = cudaMemset(h->base + h->plan.header_bytes + (int64_t)l * h->plan.layer_bytes + h->plan.ctr_off, 0,
+      e = cudaMemset(h->base + h->plan.layer[l].base + h->plan.layer[l].ctr_off, 0,
                      (size_t)h->plan.n_streams * 4);
       if (e != cudaSuccess) return cuda_fail(e, "cudaMemset counters");
     }

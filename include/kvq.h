@@ -157,6 +157,20 @@ KVQ_API kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes);
 KVQ_API kvq_status kvq_cache_create(const kvq_config* cfg, void* dev_buf, size_t bytes,
                             void* stream, kvq_cache** out);
 
+/* Per-layer code widths (mixed precision by layer: more bits for the layers
+ * whose attention is most sensitive; [TurboQuant-mem] §5.3, [KVQuant] §4.2).
+ * layer_bits: NULL (every layer uses cfg->k_bits / cfg->v_bits, as
+ * kvq_cache_bytes / kvq_cache_create) or num_layers pairs (k_bits, v_bits),
+ * layer by layer; each pair must be valid with cfg's modes and groups. The
+ * array is read during the call only. Modes, groups, outliers and capacity
+ * stay common to all layers; kvq_cache_get_layout reports each layer's own
+ * word counts and strides. */
+KVQ_API kvq_status kvq_cache_bytes_per_layer(const kvq_config* cfg, const int32_t* layer_bits,
+                                             size_t* bytes);
+KVQ_API kvq_status kvq_cache_create_per_layer(const kvq_config* cfg, const int32_t* layer_bits,
+                                              void* dev_buf, size_t bytes, void* stream,
+                                              kvq_cache** out);
+
 /* Frees the host handle only; the device buffer stays the caller's. */
 KVQ_API kvq_status kvq_cache_destroy(kvq_cache* cache);
 

@@ -103,3 +103,32 @@ def test_null_handle_is_rejected(lib):
     n = ctypes.c_int32()
     assert lib.kvq_cache_length(None, 0, ctypes.byref(n)) == 1
     assert lib.kvq_cache_status(None, None, None) == 1
+
+
+def test_per_layer_code_widths_size_the_cache(lib):
+    """A per-layer map of code widths (mixed precision by layer) sizes the
+    cache as the header plus each layer's own size; NULL is the uniform cache."""
+    def nbytes(fn, cfg, arr):
+        n = ctypes.c_size_t()
+        kvq.check(fn(ctypes.byref(cfg), arr, ctypes.byref(n)))
+        return n.value
+    base = dict(batch=2, num_kv_heads=4, head_dim=128, max_seq=1000, k_mode=kvq.ASYM_PER_CHANNEL,
+                v_mode=kvq.ASYM_PER_TOKEN, k_group=64, v_group=128, outliers_per_row=0)
+    pairs = [(8, 8), (4, 8), (4, 4), (3, 3)]
+    cfg = kvq.make_config(num_layers=4, k_bits=4, v_bits=4, **base)
+    arr = (ctypes.c_int32 * 8)(*[b for p in pairs for b in p])
+    uniform = ctypes.c_size_t()
+    kvq.check(lib.kvq_cache_bytes(ctypes.byref(cfg), ctypes.byref(uniform)))
+    assert nbytes(lib.kvq_cache_bytes_per_layer, cfg, None) == uniform.value
+    header = 256
+    want = header
+    for kb, vb in pairs:
+        one = kvq.make_config(num_layers=1, k_bits=kb, v_bits=vb, **base)
+        want += nbytes(lib.kvq_cache_bytes_per_layer, one, None) - header
+    assert nbytes(lib.kvq_cache_bytes_per_layer, cfg, arr) == want
+    # a pair that the modes and groups do not allow: 3-bit values need whole-row groups
+    bad = kvq.make_config(num_layers=2, k_bits=4, v_bits=4, **dict(base, v_group=64))
+    arr2 = (ctypes.c_int32 * 4)(4, 4, 4, 3)
+    with pytest.raises(kvq.KVQError) as e:
+        nbytes(lib.kvq_cache_bytes_per_layer, bad, arr2)
+    assert "layer 1" in str(e.value)
