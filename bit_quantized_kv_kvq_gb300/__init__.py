@@ -43,7 +43,7 @@ class KVQError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_layers", "batch", "num_kv_heads", "head_dim", "max_seq", "k_bits", "v_bits",
-        "k_mode", "v_mode", "k_group", "v_group", "outliers_per_row")]
+        "k_mode", "v_mode", "k_group", "v_group", "outliers_per_row", "sink_tokens")]
 
 
 class Layout(ctypes.Structure):
@@ -56,7 +56,9 @@ class Layout(ctypes.Structure):
             "out_col_stream_bytes", "out_val_stream_bytes")] + [
         (n, ctypes.c_void_p) for n in (
             "k_codes", "k_meta", "k_resid", "v_codes", "v_meta", "k_out_rowptr", "k_out_col",
-            "k_out_val", "v_out_rowptr", "v_out_col", "v_out_val")]
+            "k_out_val", "v_out_rowptr", "v_out_col", "v_out_val")] + [
+        ("sink_tokens", ctypes.c_int32), ("sink_len", ctypes.c_int32), ("sink_stream_bytes", ctypes.c_int64),
+        ("k_sink", ctypes.c_void_p), ("v_sink", ctypes.c_void_p)]
 
 
 _P = ctypes.c_void_p
@@ -145,9 +147,9 @@ def _stream_ptr(stream):
 
 
 def make_config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits, k_mode,
-                v_mode, k_group, v_group, outliers_per_row=0):
+                v_mode, k_group, v_group, outliers_per_row=0, sink_tokens=0):
     return Config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits, k_mode,
-                  v_mode, k_group, v_group, outliers_per_row)
+                  v_mode, k_group, v_group, outliers_per_row, sink_tokens)
 
 
 def cache_bytes(cfg: Config) -> int:
@@ -171,11 +173,11 @@ class QuantizedKVCache:
 
     def __init__(self, num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits,
                  k_mode, v_mode, k_group, v_group, outliers_per_row=0, device=None,
-                 stream=None, layer_bits=None):
+                 stream=None, layer_bits=None, sink_tokens=0):
         """layer_bits: None, or one (k_bits, v_bits) pair per layer overriding
         k_bits / v_bits (kvq_cache_create_per_layer)."""
         self.cfg = make_config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits,
-                               v_bits, k_mode, v_mode, k_group, v_group, outliers_per_row)
+                               v_bits, k_mode, v_mode, k_group, v_group, outliers_per_row, sink_tokens)
         self.layer_bits = None
         lb = None
         if layer_bits is not None:

@@ -6,6 +6,7 @@
 #include <cstring>
 
 #include "decode_impl.cuh"
+#include "decode_merge.cuh"
 #include "decode_pipe.cuh"
 
 namespace kvq {
@@ -13,7 +14,7 @@ namespace {
 
 __global__ void __launch_bounds__(kHeadDim)
     combine_kernel(const float* __restrict__ part_o, const float* __restrict__ part_ml,
-                   int splits, void* out, int out_dtype) {
+                   int splits, void* out, int out_dtype, const float* sink_part) {
   const int64_t r = blockIdx.x;
   const int c = threadIdx.x;
   const float* ml = part_ml + r * splits * 2;
@@ -25,7 +26,7 @@ __global__ void __launch_bounds__(kHeadDim)
     lsum += w * ml[2 * i + 1];
     o += w * part_o[(r * splits + i) * kHeadDim + c];
   }
-  const float res = o / lsum;
+  const float res = finish_row(sink_part, r, c, o, M, lsum);
   if (out_dtype == KVQ_F32)
     reinterpret_cast<float*>(out)[r * kHeadDim + c] = res;
   else
@@ -112,6 +113,7 @@ cudaError_t launch_decode_pipe(const LayerDev& L, const DecodeArgs& d, const Pip
   pipe::Args a;
   std::memset(&a, 0, sizeof a);
   a.q = d.q;
+  a.sink_part = d.sink_part;
   a.out = d.out;
   a.part = d.part_o;
   a.counters = L.counters;
@@ -172,7 +174,7 @@ cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t s
   if (e != cudaSuccess || a.occupancy_out) return e;
   count_launches(1);
   if (!combine) return cudaSuccess;
-  combine_kernel<<<rows, kHeadDim, 0, st>>>(a.part_o, a.part_ml, a.splits, a.out, a.out_dtype);
+  combine_kernel<<<rows, kHeadDim, 0, st>>>(a.part_o, a.part_ml, a.splits, a.out, a.out_dtype, a.sink_part);
   e = cudaGetLastError();
   if (e == cudaSuccess) count_launches(1);
   return e;

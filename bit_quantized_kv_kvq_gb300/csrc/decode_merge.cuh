@@ -7,6 +7,28 @@
 
 namespace kvq {
 
+// The output value of channel c of (batch, query head) row `row` from the
+// decode's unnormalised sum o = sum_t 2^(s_t - M) v_t, its maximum M (log2
+// units) and its weight sum lsum, merged by the log-sum-exp rule with the
+// row's attention over the fp16 sink tokens when there is one (sink_part:
+// [rows][kSinkPartRow] = o_s[128], m_s, l_s; NULL when the layer has none).
+__device__ __forceinline__ float finish_row(const float* sink_part, int64_t row, int c, float o, float M,
+                                            float lsum) {
+  if (!sink_part) return o / lsum;
+  const float* sp = sink_part + row * kSinkPartRow;
+  const float ms = __ldcg(sp + kHeadDim), ls = __ldcg(sp + kHeadDim + 1);
+  const float Mx = fmaxf(M, ms);
+  const float wa = M == -INFINITY ? 0.0f : exp2f(M - Mx);
+  const float wb = ms == -INFINITY ? 0.0f : exp2f(ms - Mx);
+  return fmaf(o, wa, __ldcg(sp + c) * wb) / fmaf(lsum, wa, ls * wb);
+}
+
+__device__ __forceinline__ float4 finish_row4(const float* sink_part, int64_t row, int c0, float4 o, float M,
+                                              float lsum) {
+  return make_float4(finish_row(sink_part, row, c0, o.x, M, lsum), finish_row(sink_part, row, c0 + 1, o.y, M, lsum),
+                     finish_row(sink_part, row, c0 + 2, o.z, M, lsum), finish_row(sink_part, row, c0 + 3, o.w, M, lsum));
+}
+
 // Split-K merge at the end of the kernel. Every CTA of a stream, once its
 // partials are written and fenced, adds one to the stream's arrival counter;
 // the CTA that arrives last merges the partials of the stream's G query rows
@@ -72,12 +94,12 @@ __device__ __forceinline__ void merge_splits_if_last(uint32_t* counter, const De
       }
     }
     const int64_t o = prow * kHeadDim + 4 * lane;
+    const float4 r = finish_row4(a.sink_part, prow, 4 * lane, acc, M, lsum);
     if (a.out_dtype == KVQ_F32) {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + o) =
-          make_float4(acc.x / lsum, acc.y / lsum, acc.z / lsum, acc.w / lsum);
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + o) = r;
     } else {
-      const __half2 h01 = __floats2half2_rn(acc.x / lsum, acc.y / lsum);
-      const __half2 h23 = __floats2half2_rn(acc.z / lsum, acc.w / lsum);
+      const __half2 h01 = __floats2half2_rn(r.x, r.y);
+      const __half2 h23 = __floats2half2_rn(r.z, r.w);
       uint2 u;
       u.x = *reinterpret_cast<const uint32_t*>(&h01);
       u.y = *reinterpret_cast<const uint32_t*>(&h23);

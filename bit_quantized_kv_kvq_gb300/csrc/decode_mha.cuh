@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 4)
     lsum = NAN;
   }
   if (a.splits == 1) {
-    const float res = o / lsum;
+    const float res = finish_row(a.sink_part, prow, c, o, M, lsum);
     if (a.out_dtype == KVQ_F32)
       reinterpret_cast<float*>(a.out)[prow * kHeadDim + c] = res;
     else

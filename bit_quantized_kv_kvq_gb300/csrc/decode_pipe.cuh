@@ -37,6 +37,7 @@
 
 #include <cuda.h>
 
+#include "decode_merge.cuh"
 #include "mma_frag.cuh"
 #include "tensor_map.cuh"
 
@@ -58,6 +59,7 @@ struct __align__(64) Maps {
 
 struct Args {
   const __half* q;      // [B][Hq][D]
+  const float* sink_part;  // attention over the fp16 sink tokens per row, or NULL
   void* out;            // [B][Hq][D]
   float* part;          // [streams][jmax][H][kPartRow]
   uint32_t* counters;   // [streams], zero between calls
@@ -824,8 +826,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (K == 1) {
         for (int h = 0; h < H; ++h) {
           const float4 o = *reinterpret_cast<const float4*>(so + h * kHeadDim + 4 * lane);
-          const float il = 1.0f / sl[h];
-          write_out(h, make_float4(o.x * il, o.y * il, o.z * il, o.w * il));
+          write_out(h, finish_row4(a.sink_part, (int64_t)b * a.num_q_heads + kvh * H + h, 4 * lane, o, sm[h], sl[h]));
         }
         return;
       }
@@ -1094,13 +1095,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           o.w = fmaf(w, v[jj].w, o.w);
         }
       }
-      const float il = 1.0f / Ls;
-      const int64_t base = ((int64_t)b * a.num_q_heads + kvh * H + h) * kHeadDim + 4 * lane;
+      const int64_t row = (int64_t)b * a.num_q_heads + kvh * H + h;
+      const int64_t base = row * kHeadDim + 4 * lane;
+      const float4 r = finish_row4(a.sink_part, row, 4 * lane, o, M, Ls);
       if (a.out_dtype == KVQ_F32) {
-        *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + base) =
-            make_float4(o.x * il, o.y * il, o.z * il, o.w * il);
+        *reinterpret_cast<float4*>(reinterpret_cast<float*>(a.out) + base) = r;
       } else {
-        __half2 h01 = __floats2half2_rn(o.x * il, o.y * il), h23 = __floats2half2_rn(o.z * il, o.w * il);
+        __half2 h01 = __floats2half2_rn(r.x, r.y), h23 = __floats2half2_rn(r.z, r.w);
         uint2 u;
         u.x = *reinterpret_cast<uint32_t*>(&h01);
         u.y = *reinterpret_cast<uint32_t*>(&h23);

@@ -942,7 +942,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
     }
     const int64_t prow = (int64_t)b * a.num_q_heads + hq0 + h;
     if (a.splits == 1) {
-      const float res = ov / lsum;
+      const float res = finish_row(a.sink_part, prow, c, ov, M, lsum);
       if (a.out_dtype == KVQ_F32)
         reinterpret_cast<float*>(a.out)[prow * kHeadDim + c] = res;
       else

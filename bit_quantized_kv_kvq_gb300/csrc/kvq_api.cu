@@ -62,6 +62,7 @@ struct TensorPlan {
 struct LayerPlan {
   int k_bits = 0, v_bits = 0;
   TensorPlan k, v;
+  int64_t sink_k_off = 0, sink_v_off = 0, sink_sb = 0;  // fp16 sink tokens [n][sink_tokens][D]
   int64_t ctr_off = 0;  // uint32 split-merge counters [n_streams]
   int64_t base = 0;     // from the start of the buffer
 };
@@ -112,6 +113,8 @@ kvq_status check_config(const kvq_config* c, const int32_t* layer_bits = nullptr
     return fail(KVQ_ERR_UNSUPPORTED, "batch * num_kv_heads must be <= 65535");
   if (c->outliers_per_row < 0 || c->outliers_per_row > kvq::kMaxOutliers)
     return fail(KVQ_ERR_INVALID_ARG, "outliers_per_row must be in [0, %d]", kvq::kMaxOutliers);
+  if (c->sink_tokens < 0 || c->sink_tokens > kvq::kMaxSinkTokens || c->sink_tokens >= c->max_seq)
+    return fail(KVQ_ERR_INVALID_ARG, "sink_tokens must be in [0, %d] and below max_seq", kvq::kMaxSinkTokens);
   kvq_status s = check_tensor("k", c->k_bits, c->k_mode, c->k_group, true);
   if (s != KVQ_OK) return s;
   s = check_tensor("v", c->v_bits, c->v_mode, c->v_group, false);
@@ -169,6 +172,13 @@ Plan make_plan(const kvq_config& c, const int32_t* layer_bits = nullptr) {
     int64_t cursor = 0;
     plan_tensor(c, lp.k_bits, p.capacity, true, &cursor, &lp.k);
     plan_tensor(c, lp.v_bits, p.capacity, false, &cursor, &lp.v);
+    if (c.sink_tokens > 0) {
+      lp.sink_sb = round_up((int64_t)c.sink_tokens * kvq::kHeadDim * 2, 256);
+      lp.sink_k_off = cursor;
+      cursor += p.n_streams * lp.sink_sb;
+      lp.sink_v_off = cursor;
+      cursor += p.n_streams * lp.sink_sb;
+    }
     lp.ctr_off = cursor;
     cursor = round_up(cursor + p.n_streams * 4, 256);
     lp.base = base;
@@ -238,8 +248,26 @@ kvq::LayerDev layer_dev(const kvq_cache* h, int layer) {
   L.capacity = h->plan.capacity;
   L.outliers = h->cfg.outliers_per_row;
   L.status = reinterpret_cast<uint32_t*>(h->base);
-  L.counters = reinterpret_cast<uint32_t*>(h->base + h->plan.layer[layer].base + h->plan.layer[layer].ctr_off);
+  const LayerPlan& lp = h->plan.layer[layer];
+  L.counters = reinterpret_cast<uint32_t*>(h->base + lp.base + lp.ctr_off);
+  L.in_rows = 0;
+  L.sink_tokens = h->cfg.sink_tokens;
+  L.sink_k = h->cfg.sink_tokens ? reinterpret_cast<__half*>(h->base + lp.base + lp.sink_k_off) : nullptr;
+  L.sink_v = h->cfg.sink_tokens ? reinterpret_cast<__half*>(h->base + lp.base + lp.sink_v_off) : nullptr;
   return L;
+}
+
+// Tokens of a layer held as sinks, and the tokens after them (the coded rows).
+int sink_len(const kvq_config& c, int len) { return len < c.sink_tokens ? len : c.sink_tokens; }
+int coded_len(const kvq_config& c, int len) { return len - sink_len(c, len); }
+
+// fp16 rows [0, rows) of every stream of a [n][src_rows][D] input (or of a
+// single [n][D] row, src_rows = 1) into the sink array at row `at`.
+cudaError_t copy_sink_rows(const kvq::LayerDev& L, __half* dst, const void* src, int src_rows, int at, int rows,
+                           cudaStream_t st) {
+  const size_t row = (size_t)kvq::kHeadDim * 2;
+  return cudaMemcpy2DAsync(dst + (size_t)at * kvq::kHeadDim, (size_t)L.sink_tokens * row, src, (size_t)src_rows * row,
+                           (size_t)rows * row, (size_t)L.n_streams, cudaMemcpyDeviceToDevice, st);
 }
 
 int k_quant_len(const kvq_config& c, int len) {
@@ -281,6 +309,12 @@ void plan_splits(const kvq_cache* h, int len, int slots, int* splits, int* tiles
   }
   *splits = best_s;
   *tiles_per_split = best_tps;
+}
+
+// Workspace bytes of the sink partials (at the front of the workspace).
+size_t sink_part_bytes(const kvq_cache* h, int num_q_heads) {
+  if (h->cfg.sink_tokens == 0) return 0;
+  return (size_t)round_up((int64_t)h->cfg.batch * num_q_heads * kvq::kSinkPartRow * 4, 256);
 }
 
 size_t workspace_for(const kvq_cache* h, int num_q_heads, int splits) {
@@ -381,11 +415,19 @@ kvq_status kvq_prefill_quantize(kvq_cache* h, int32_t layer, const void* k, cons
       return fail(KVQ_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
   }
   kvq::LayerDev L = layer_dev(h, layer);
-  cudaError_t e = kvq::launch_prefill(L, static_cast<const __half*>(k),
-                                      static_cast<const __half*>(v), seq_len,
-                                      static_cast<cudaStream_t>(stream));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int ns = sink_len(h->cfg, seq_len), nq = seq_len - ns;
+  if (ns > 0) {  // the first tokens stay in fp16
+    cudaError_t e = copy_sink_rows(L, L.sink_k, k, seq_len, 0, ns, st);
+    if (e == cudaSuccess) e = copy_sink_rows(L, L.sink_v, v, seq_len, 0, ns, st);
+    if (e != cudaSuccess) return cuda_fail(e, "sink copy");
+  }
+  L.in_rows = seq_len;
+  const __half* kq = seq_len > 0 ? static_cast<const __half*>(k) + (size_t)ns * kvq::kHeadDim : nullptr;
+  const __half* vq = seq_len > 0 ? static_cast<const __half*>(v) + (size_t)ns * kvq::kHeadDim : nullptr;
+  cudaError_t e = kvq::launch_prefill(L, kq, vq, nq, st);
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
-  if (seq_len > 0) kvq::count_launches(1);
+  if (nq > 0) kvq::count_launches(1);
   h->len[layer] = seq_len;
   return KVQ_OK;
 }
@@ -403,11 +445,17 @@ kvq_status kvq_append_quantize(kvq_cache* h, int32_t layer, const void* k, const
   if (pos >= h->cfg.max_seq)
     return fail(KVQ_ERR_CAPACITY, "layer %d is full (%d tokens)", layer, pos);
   kvq::LayerDev L = layer_dev(h, layer);
-  cudaError_t e = kvq::launch_append(L, static_cast<const __half*>(k),
-                                     static_cast<const __half*>(v), pos,
-                                     static_cast<cudaStream_t>(stream));
-  if (e != cudaSuccess) return cuda_fail(e, "append launch");
-  kvq::count_launches(1);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (pos < h->cfg.sink_tokens) {  // a sink token: kept in fp16 as it is
+    cudaError_t e = copy_sink_rows(L, L.sink_k, k, 1, pos, 1, st);
+    if (e == cudaSuccess) e = copy_sink_rows(L, L.sink_v, v, 1, pos, 1, st);
+    if (e != cudaSuccess) return cuda_fail(e, "sink copy");
+  } else {
+    cudaError_t e = kvq::launch_append(L, static_cast<const __half*>(k), static_cast<const __half*>(v),
+                                       pos - h->cfg.sink_tokens, st);
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    kvq::count_launches(1);
+  }
   h->len[layer] = pos + 1;
   return KVQ_OK;
 }
@@ -433,7 +481,7 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* h, int32_t num_q_heads, s
     const size_t b = workspace_for(h, num_q_heads, max_splits);
     if (b > need) need = b;
   }
-  *bytes = need;
+  *bytes = need + sink_part_bytes(h, num_q_heads);
   return KVQ_OK;
 }
 
@@ -454,16 +502,36 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
     return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d",
                 num_q_heads, hkv);
   const int gqa = num_q_heads / hkv;
-  const int len = h->len[layer];
+  int len = h->len[layer];
   if (len == 0) return fail(KVQ_ERR_INVALID_ARG, "layer %d is empty: attention is undefined", layer);
   kvq::LayerDev L = layer_dev(h, layer);
   if (!kvq::decode_supported(L, gqa))
     return fail(KVQ_ERR_UNSUPPORTED, "no decode kernel for this codec pair with %d query heads per kv-head",
                 gqa);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float scale_log2 = softmax_scale * 1.4426950408889634f;
+  // fp16 sink tokens first: their attention is merged into the decode's output
+  // (or is the output when no token is coded yet)
+  const int nsink = sink_len(h->cfg, len), ncoded = len - nsink;
+  const size_t sink_ws = sink_part_bytes(h, num_q_heads);
+  if (ws_bytes < sink_ws)
+    return fail(KVQ_ERR_BUFFER_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, sink_ws);
+  float* sink_part = nullptr;
+  if (nsink > 0) {
+    sink_part = static_cast<float*>(workspace);
+    cudaError_t e = kvq::launch_sink_attention(L, static_cast<const __half*>(q), num_q_heads, scale_log2, nsink,
+                                               sink_part, ncoded == 0 ? out : nullptr, out_dtype, st);
+    if (e != cudaSuccess) return cuda_fail(e, "sink attention launch");
+    if (ncoded == 0) return KVQ_OK;
+  }
+  workspace = static_cast<unsigned char*>(workspace) + sink_ws;
+  ws_bytes -= sink_ws;
+  len = ncoded;
   kvq::DecodeArgs a;
   std::memset(&a, 0, sizeof a);
   a.gqa = gqa;
   a.num_q_heads = num_q_heads;
+  a.sink_part = sink_part;
   if (kvq::decode_pipe_supported(L, gqa)) {
     const kvq::PipePlan pp = kvq::plan_decode_pipe(L, len, gqa, h->sm_count, h->splits_override);
     if (ws_bytes < pp.ws_bytes)
@@ -475,13 +543,13 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
     a.length = len;
     a.k_quant_len = k_quant_len(h->cfg, len);
     a.part_o = static_cast<float*>(workspace);
-    cudaError_t e = kvq::launch_decode_pipe(L, a, pp, static_cast<cudaStream_t>(stream));
+    cudaError_t e = kvq::launch_decode_pipe(L, a, pp, st);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return KVQ_OK;
   }
   int occ = 0;
   a.occupancy_out = &occ;
-  cudaError_t e = kvq::launch_decode(L, a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = kvq::launch_decode(L, a, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode occupancy query");
   a.occupancy_out = nullptr;
   int splits = 1, tps = 1;
@@ -502,7 +570,7 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
   const int64_t rows = (int64_t)h->cfg.batch * num_q_heads;
   a.part_o = static_cast<float*>(workspace);
   a.part_ml = a.part_o + rows * splits * kvq::kHeadDim;
-  e = kvq::launch_decode(L, a, static_cast<cudaStream_t>(stream));
+  e = kvq::launch_decode(L, a, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return KVQ_OK;
 }
@@ -523,8 +591,13 @@ kvq_status kvq_cache_get_layout(const kvq_cache* h, int32_t layer, kvq_layout* o
   kvq::LayerDev L = layer_dev(h, layer);
   o->capacity = h->plan.capacity;
   o->length = len;
-  o->k_quantized_len = k_quant_len(h->cfg, len);
-  o->k_resid_len = len - o->k_quantized_len;
+  o->k_quantized_len = k_quant_len(h->cfg, coded_len(h->cfg, len));
+  o->k_resid_len = coded_len(h->cfg, len) - o->k_quantized_len;
+  o->sink_tokens = h->cfg.sink_tokens;
+  o->sink_len = sink_len(h->cfg, len);
+  o->sink_stream_bytes = h->plan.layer[layer].sink_sb;
+  o->k_sink = L.sink_k;
+  o->v_sink = L.sink_v;
   const LayerPlan& lp = h->plan.layer[layer];
   o->k_words_per_row = lp.k.words;
   o->v_words_per_row = lp.v.words;

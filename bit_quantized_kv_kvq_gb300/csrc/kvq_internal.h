@@ -45,7 +45,13 @@ struct LayerDev {
   int outliers;         // per row
   uint32_t* status;
   uint32_t* counters;   // [n_streams] split-merge counters of the layer, zero between calls
+  int in_rows;          // prefill: input rows per stream (0: the rows quantized)
+  int sink_tokens;      // fp16 attention-sink tokens per stream (0: none)
+  __half* sink_k;       // [n][sink_tokens][D]
+  __half* sink_v;       // [n][sink_tokens][D]
 };
+
+constexpr int kMaxSinkTokens = 64;
 
 // Prefill of seq_len tokens: k, v fp16 [n][seq_len][D].
 cudaError_t launch_prefill(const LayerDev& L, const __half* k, const __half* v, int seq_len,
@@ -58,6 +64,7 @@ cudaError_t launch_append(const LayerDev& L, const __half* k1, const __half* v1,
 
 struct DecodeArgs {
   const __half* q;      // [B][Hq][D]
+  const float* sink_part;  // [B*Hq][kSinkPartRow] attention over the sink tokens, or NULL
   void* out;            // [B][Hq][D]
   int out_dtype;
   int num_q_heads;
@@ -73,6 +80,15 @@ struct DecodeArgs {
 };
 
 cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);
+
+// Attention over the fp16 sink tokens of every (batch, query head) row: the
+// unnormalised partial o[128], its running max m (log2 units) and sum l, for
+// the decode kernels to merge into their output (part: [B*Hq][kSinkPartRow]);
+// with `final_out` set, the normalised output itself (no other tokens).
+constexpr int kSinkPartRow = 132;  // o[128], m, l, pad
+cudaError_t launch_sink_attention(const LayerDev& L, const __half* q, int num_q_heads, float scale_log2,
+                                  int sink_len, float* part, void* final_out, int out_dtype,
+                                  cudaStream_t stream);
 
 bool decode_supported(const LayerDev& L, int gqa);
 

@@ -851,6 +851,7 @@ struct Args {
   const __half* ksrc;
   const __half* vsrc;
   int seq_len;
+  int in_rows;  // input rows between streams (>= seq_len)
   int k_items;  // key items per stream: whole blocks (+1 residual copy) or row chunks
   int k_nfull;  // whole per-channel key blocks per stream
   int v_items;  // value row chunks per stream
@@ -939,7 +940,7 @@ __global__ void __launch_bounds__(32 * Geo<KB, KMODE, TB, VB, OUTL>::kW, (Geo<KB
     mbar_arrive_expect_tx(&full[s], bytes);
     if (bytes)
       bulk_g2s(smem + (size_t)s * G::kStageBytes,
-               src + ((int64_t)r.n * a.seq_len + r.row0) * kHeadDim, bytes, &full[s]);
+               src + ((int64_t)r.n * a.in_rows + r.row0) * kHeadDim, bytes, &full[s]);
   };
 
   if (tid == 0) {
@@ -975,7 +976,7 @@ __global__ void __launch_bounds__(32 * Geo<KB, KMODE, TB, VB, OUTL>::kW, (Geo<KB
       if (r.kind == 1) {
         // key residual: the last S mod T tokens stay fp16
         const int t0 = a.k_nfull * TB;
-        const uint4* s4 = reinterpret_cast<const uint4*>(a.ksrc + ((int64_t)r.n * a.seq_len + t0) * kHeadDim);
+        const uint4* s4 = reinterpret_cast<const uint4*>(a.ksrc + ((int64_t)r.n * a.in_rows + t0) * kHeadDim);
         uint4* d4 = reinterpret_cast<uint4*>(a.k.resid + (int64_t)r.n * a.k.resid_sstride);
         const int count = (a.seq_len - t0) * (kHeadDim / 8);
         for (int i = tid; i < count; i += 32 * W) d4[i] = s4[i];
@@ -1031,6 +1032,7 @@ cudaError_t launch_fast_t(const LayerDev& L, const __half* k, const __half* v, i
   a.ksrc = k;
   a.vsrc = v;
   a.seq_len = seq_len;
+  a.in_rows = L.in_rows > 0 ? L.in_rows : seq_len;
   a.n_streams = L.n_streams;
   a.kout = OUTL ? L.outliers : 0;
   a.status = L.status;

@@ -745,8 +745,8 @@ __device__ __forceinline__ void kblock_item(const uint4* __restrict__ tile, cons
 }
 
 __device__ __forceinline__ void resid_copy(const TensorDev& K, const __half* __restrict__ src,
-                                           int n, int t0, int seq_len) {
-  const uint4* s4 = reinterpret_cast<const uint4*>(src + ((int64_t)n * seq_len + t0) * kHeadDim);
+                                           int n, int t0, int seq_len, int in_rows) {
+  const uint4* s4 = reinterpret_cast<const uint4*>(src + ((int64_t)n * in_rows + t0) * kHeadDim);
   uint4* d4 = reinterpret_cast<uint4*>(K.resid + (int64_t)n * K.resid_sstride);
   const int count = (seq_len - t0) * (kHeadDim / 8);
   for (int i = threadIdx.x; i < count; i += kThreads) d4[i] = s4[i];
@@ -757,6 +757,7 @@ struct PrefillArgs {
   const __half* ksrc;
   const __half* vsrc;
   int seq_len;
+  int in_rows;  // input rows between streams (>= seq_len)
   int kout;
   int k_items;  // key items per stream: whole blocks (+1 residual copy) or 64-row chunks
   int k_nfull;  // whole per-channel key blocks per stream
@@ -832,7 +833,7 @@ __global__ void __launch_bounds__(kThreads, (KR >= 16 ? 1 : 3)) prefill_kernel(P
     const uint32_t bytes = (uint32_t)r.nrows * kHeadDim * 2;
     mbar_arrive_expect_tx(&bars[s], bytes);
     if (bytes)
-      bulk_g2s(smem + (size_t)s * G::kStage, src + ((int64_t)r.n * a.seq_len + r.row0) * kHeadDim,
+      bulk_g2s(smem + (size_t)s * G::kStage, src + ((int64_t)r.n * a.in_rows + r.row0) * kHeadDim,
                bytes, &bars[s]);
   };
 
@@ -866,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, (KR >= 16 ? 1 : 3)) prefill_kernel(P
         kblock_item<KB, KR>(tile, a.k, r.n, r.idx, a.kout,
                             *reinterpret_cast<KBlockSmem<KB, KR>*>(scratch));
     } else if (r.kind == 1) {
-      resid_copy(a.k, a.ksrc, r.n, a.k_nfull * T, a.seq_len);
+      resid_copy(a.k, a.ksrc, r.n, a.k_nfull * T, a.seq_len, a.in_rows);
     } else if (r.kind == 2) {
       rows_item<KB, KMODE == KVQ_SYM_PER_TOKEN>(tile, a.k, r.n, r.row0, r.nrows, a.kout, scratch);
     } else {
@@ -901,6 +902,7 @@ cudaError_t launch_prefill_t(const LayerDev& L, const __half* k, const __half* v
   a.ksrc = k;
   a.vsrc = v;
   a.seq_len = seq_len;
+  a.in_rows = L.in_rows > 0 ? L.in_rows : seq_len;
   a.kout = L.outliers;
   a.n_streams = L.n_streams;
   a.status = L.status;

@@ -100,6 +100,11 @@ typedef struct kvq_config {
   int32_t outliers_per_row; /* 0 = dense only; 1..8 fp16 outliers per (token, head)
                                row, chosen by |x| descending, ties to the lower channel
                                ([KVQuant] §2.2 item 3, §3.3)                             */
+  int32_t sink_tokens;      /* 0..64: the first sink_tokens tokens of every stream are
+                               kept in fp16 for keys and values and take part in
+                               attention as they are ("attention sinks", [KVQuant]
+                               §4.1, which keeps the first 5-10); quantization (and
+                               the per-channel key blocks) starts after them         */
 } kvq_config;
 
 /* Packed layout of one layer, for inspection (parity tests, checkpoints).
@@ -122,7 +127,7 @@ typedef struct kvq_config {
  *      an outlier slot is 0. NULL when outliers_per_row == 0. */
 typedef struct kvq_layout {
   int32_t capacity;           /* rows per stream (max_seq rounded up)              */
-  int32_t length;             /* tokens cached in this layer                       */
+  int32_t length;             /* tokens cached in this layer (sinks included)      */
   int32_t k_quantized_len;    /* key rows held as codes                            */
   int32_t k_resid_len;        /* key rows held in the fp16 residual                */
   int32_t k_words_per_row, v_words_per_row;
@@ -142,6 +147,14 @@ typedef struct kvq_layout {
   void* v_out_rowptr;
   void* v_out_col;
   void* v_out_val;
+  /* attention sinks: fp16 keys and values [n][sink_tokens][D] each; the first
+   * sink_len rows are live. The coded rows (k_quantized_len, k_resid_len and
+   * the value rows, length - sink_len of them) start after the sinks. */
+  int32_t sink_tokens;
+  int32_t sink_len;
+  int64_t sink_stream_bytes;
+  void* k_sink;
+  void* v_sink;
 } kvq_layout;
 
 typedef struct kvq_cache kvq_cache; /* opaque host-side handle */
@@ -194,7 +207,8 @@ KVQ_API kvq_status kvq_append_quantize(kvq_cache* cache, int32_t layer, const vo
                                const void* v, void* stream);
 
 /* Workspace bytes kvq_decode_attention needs for `num_q_heads` query heads
- * at any length up to max_seq (the split partials). Host only. */
+ * at any length up to max_seq (the split partials, and the attention over
+ * the sink tokens when the cache keeps some). Host only. */
 KVQ_API kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t num_q_heads,
                                       size_t* bytes);
 
@@ -214,7 +228,9 @@ KVQ_API kvq_status kvq_decode_workspace_bytes(const kvq_cache* cache, int32_t nu
  * With 8 query heads per kv-head (per-channel keys, per-token values) the
  * decode is one persistent launch over all streams (stream-K: the key blocks
  * of all streams cut into one range per SM), otherwise one CTA per (split,
- * stream).
+ * stream). When the layer holds sink tokens (cfg.sink_tokens), a first small
+ * launch computes the attention over them and the decode merges it into its
+ * output (log-sum-exp); with only sink tokens cached it writes the output.
  * Errors: KVQ_ERR_INVALID_ARG when the layer is empty;
  * KVQ_ERR_BUFFER_TOO_SMALL for a short workspace. */
 KVQ_API kvq_status kvq_decode_attention(kvq_cache* cache, int32_t layer, const void* q,
@@ -266,7 +282,9 @@ KVQ_API const char* kvq_last_error(void);
 
 /* Number of device kernels this process has enqueued through the library
  * (all caches, all threads), counted on the host at each successful
- * launch: prefill 1, append 1, decode 1 (the split partials are merged by
+ * launch: prefill 1 (none when every token is a sink), append 1 (none for a
+ * sink token: it is copied), decode 1 plus 1 for the sink attention when
+ * the layer holds sink tokens (the split partials are merged by
  * the last CTA of each stream inside the decode kernel), except the generic
  * decode used for the rarer codec combinations (per-token keys with
  * outliers, sub-32-channel groups), which adds 1 for a combine launch;

@@ -261,6 +261,7 @@ class CodecSpec:
     k_group: int
     v_group: int
     outliers_per_row: int = 0
+    sink_tokens: int = 0
 
 
 class TensorState:
@@ -348,6 +349,12 @@ class OracleCache:
     keys; codes already written are never requantized. Values (and keys in
     per-token modes) are quantized row by row as they arrive ([NIAH-q8_0]
     §2.2: only the newly written row is quantized).
+
+    Attention sinks ([KVQuant] §4.1: the first 5-10 tokens keep full
+    precision; reading R18): the first ``spec.sink_tokens`` tokens of every
+    stream keep their fp16 keys and values, take part in attention as they
+    are, and are never quantized; quantization, and the per-channel key
+    blocks, start at the token after them.
     """
 
     def __init__(self, spec: CodecSpec, n_streams: int):
@@ -356,6 +363,14 @@ class OracleCache:
         self.length = 0
         self.k = None
         self.v = None
+        d = spec.head_dim
+        self.sink_k = np.zeros((n_streams, 0, d), np.float16)
+        self.sink_v = np.zeros((n_streams, 0, d), np.float16)
+
+    @property
+    def coded_length(self):
+        """Tokens after the sinks (the quantized rows and the key residual)."""
+        return self.length - self.sink_k.shape[1]
 
     # -- helpers --------------------------------------------------------
     def _empty_state(self, bits, mode, group):
@@ -398,8 +413,11 @@ class OracleCache:
         assert k16.shape[2] == sp.head_dim
         self.k = self._empty_state(sp.k_bits, sp.k_mode, sp.k_group)
         self.v = self._empty_state(sp.v_bits, sp.v_mode, sp.v_group)
-        self._append_rows(self.k, k16, sp.k_bits, sp.k_mode, sp.k_group)
-        self._append_rows(self.v, v16, sp.v_bits, sp.v_mode, sp.v_group)
+        ns = min(k16.shape[1], sp.sink_tokens)
+        self.sink_k = k16[:, :ns].copy()
+        self.sink_v = v16[:, :ns].copy()
+        self._append_rows(self.k, k16[:, ns:], sp.k_bits, sp.k_mode, sp.k_group)
+        self._append_rows(self.v, v16[:, ns:], sp.v_bits, sp.v_mode, sp.v_group)
         self.length = k16.shape[1]
 
     def append(self, k1, v1):
@@ -410,8 +428,12 @@ class OracleCache:
             self.v = self._empty_state(sp.v_bits, sp.v_mode, sp.v_group)
         k1 = np.asarray(k1, np.float16)[:, None, :]
         v1 = np.asarray(v1, np.float16)[:, None, :]
-        self._append_rows(self.k, k1, sp.k_bits, sp.k_mode, sp.k_group)
-        self._append_rows(self.v, v1, sp.v_bits, sp.v_mode, sp.v_group)
+        if self.length < sp.sink_tokens:
+            self.sink_k = np.concatenate([self.sink_k, k1], axis=1)
+            self.sink_v = np.concatenate([self.sink_v, v1], axis=1)
+        else:
+            self._append_rows(self.k, k1, sp.k_bits, sp.k_mode, sp.k_group)
+            self._append_rows(self.v, v1, sp.v_bits, sp.v_mode, sp.v_group)
         self.length += 1
 
     # -- dequantization (fp64) --------------------------------------------
@@ -435,14 +457,17 @@ class OracleCache:
             np.put_along_axis(xh, st.out_cols, st.out_vals.astype(np.float64), axis=2)
         if st.resid is not None and st.resid.shape[1]:
             xh = np.concatenate([xh, st.resid.astype(np.float64)], axis=1)
-        assert xh.shape == (n, self.length, d)
+        assert xh.shape == (n, self.coded_length, d)
         return xh
 
     def dequant_k(self):
-        return self._dequant(self.k, self.spec.k_mode, self.spec.k_group)
+        """Every cached key in fp64: the fp16 sinks, then the dequantized rows."""
+        return np.concatenate([self.sink_k.astype(np.float64),
+                               self._dequant(self.k, self.spec.k_mode, self.spec.k_group)], axis=1)
 
     def dequant_v(self):
-        return self._dequant(self.v, self.spec.v_mode, self.spec.v_group)
+        return np.concatenate([self.sink_v.astype(np.float64),
+                               self._dequant(self.v, self.spec.v_mode, self.spec.v_group)], axis=1)
 
     def decode(self, q, softmax_scale):
         """Decode attention of q [N][g][D] (g query heads per KV stream)

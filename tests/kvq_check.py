@@ -15,15 +15,16 @@ from oracle import kvq_oracle as O
 ATTN_TOL = 1e-3
 
 
-def spec_of(wl):
+def spec_of(wl, sink_tokens=0):
     return O.CodecSpec(wl.head_dim, wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode,
-                       wl.k_group, wl.v_group, wl.outliers_per_row)
+                       wl.k_group, wl.v_group, wl.outliers_per_row, sink_tokens)
 
 
-def make_gpu_cache(wl, max_seq, num_layers=None, device="cuda"):
+def make_gpu_cache(wl, max_seq, num_layers=None, device="cuda", sink_tokens=0):
     return kvq.QuantizedKVCache(num_layers or wl.num_layers, wl.batch, wl.num_kv_heads,
                                 wl.head_dim, max_seq, wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode,
-                                wl.k_group, wl.v_group, wl.outliers_per_row, device=device)
+                                wl.k_group, wl.v_group, wl.outliers_per_row, device=device,
+                                sink_tokens=sink_tokens)
 
 
 def streams_of(x, wl):
@@ -47,9 +48,13 @@ def gpu_state(cache, layer, n):
     c = cache.cfg
     lo = cache.layout(layer)
     D = c.head_dim
-    L = lo.length
+    L = lo.length - lo.sink_len  # coded rows (after the fp16 sinks)
     kq = lo.k_quantized_len
     out = {}
+    if lo.sink_tokens:
+        ns = lo.sink_len
+        out["k_sink"] = _bytes(cache, lo.k_sink + n * lo.sink_stream_bytes, ns * D * 2).view(np.float16).reshape(ns, D)
+        out["v_sink"] = _bytes(cache, lo.v_sink + n * lo.sink_stream_bytes, ns * D * 2).view(np.float16).reshape(ns, D)
     kr = kq if c.k_mode == O.ASYM_PER_CHANNEL else L
     wk, wv = lo.k_words_per_row, lo.v_words_per_row
     out["k_words"] = _bytes(cache, lo.k_codes + n * lo.k_codes_stream_bytes, kr * wk * 4).view(np.uint32).reshape(kr, wk)
@@ -83,6 +88,9 @@ def oracle_state(oc: O.OracleCache, i):
     """The same arrays for oracle stream i."""
     sp = oc.spec
     out = {"k_words": oc.k_words()[i], "v_words": oc.v_words()[i]}
+    if sp.sink_tokens:
+        out["k_sink"] = oc.sink_k[i]
+        out["v_sink"] = oc.sink_v[i]
     if sp.k_mode == O.ASYM_PER_CHANNEL:
         out["k_meta"] = np.stack([oc.k.scale16[i].view(np.uint16), oc.k.zero16[i].view(np.uint16)], -1)
         out["k_resid"] = oc.k.resid[i]

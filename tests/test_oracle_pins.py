@@ -596,3 +596,70 @@ def test_row_relative_error_closed_form():
     x = np.arange(24.0).reshape(2, 3, 4) + 1
     e = O.row_relative_error(x * (1 + 1e-3), x)
     assert e.shape == (2, 3) and np.allclose(e, 1e-3, rtol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Attention sinks ([KVQuant] §4.1): the first tokens kept in fp16
+# ---------------------------------------------------------------------------
+
+def _sink_spec(ns, kmode=O.ASYM_PER_CHANNEL, bits=3):
+    return O.CodecSpec(128, bits, bits, kmode, O.ASYM_PER_TOKEN, 64 if kmode == O.ASYM_PER_CHANNEL else 32,
+                       128, 0, ns)
+
+
+def test_all_sink_cache_is_exact_attention():
+    """When the sinks cover the whole sequence nothing is quantized: the
+    decode is fp64 attention on the fp16 inputs themselves."""
+    rng = np.random.default_rng(91)
+    k = rng.standard_normal((2, 7, 128)).astype(np.float16)
+    v = rng.standard_normal((2, 7, 128)).astype(np.float16)
+    q = rng.standard_normal((2, 3, 128))
+    c = O.OracleCache(_sink_spec(8), 2)
+    c.prefill(k, v)
+    assert c.coded_length == 0 and c.sink_k.shape[1] == 7
+    assert np.array_equal(c.decode(q, 0.1), O.attend(q, k.astype(np.float64), v.astype(np.float64), 0.1))
+
+
+@pytest.mark.parametrize("kmode", [O.ASYM_PER_CHANNEL, O.ASYM_PER_TOKEN])
+def test_sinks_shift_quantization_past_them(kmode):
+    """With sinks, the quantized state is that of a cache without sinks fed
+    the tokens after them (per-channel key blocks start after the sinks), by
+    prefill and by appends crossing the sink boundary alike."""
+    rng = np.random.default_rng(92 + kmode)
+    ns, s = 5, 200
+    k = rng.standard_normal((2, s, 128)).astype(np.float16)
+    v = rng.standard_normal((2, s, 128)).astype(np.float16)
+    a = O.OracleCache(_sink_spec(ns, kmode), 2)
+    a.prefill(k, v)
+    b = O.OracleCache(_sink_spec(0, kmode), 2)
+    b.prefill(k[:, ns:], v[:, ns:])
+    assert np.array_equal(a.sink_k, k[:, :ns]) and np.array_equal(a.sink_v, v[:, :ns])
+    for f in ("codes", "scale16", "zero16"):
+        assert np.array_equal(getattr(a.k, f), getattr(b.k, f)), f
+        assert np.array_equal(getattr(a.v, f), getattr(b.v, f)), f
+    c = O.OracleCache(_sink_spec(ns, kmode), 2)
+    c.prefill(k[:, :3], v[:, :3])
+    for t in range(3, s):
+        c.append(k[:, t], v[:, t])
+    assert np.array_equal(c.k.codes, b.k.codes) and np.array_equal(c.v.codes, b.v.codes)
+    assert np.array_equal(c.sink_k, a.sink_k)
+    q = rng.standard_normal((2, 2, 128))
+    assert np.array_equal(c.decode(q, 0.09), a.decode(q, 0.09))
+
+
+def test_sinks_keep_a_dominant_first_token_exact():
+    """A first token that draws most of the attention (the pattern that
+    motivates sinks) is reproduced better with it kept in fp16."""
+    rng = np.random.default_rng(93)
+    s = 256
+    k = rng.standard_normal((1, s, 128)).astype(np.float16)
+    v = rng.standard_normal((1, s, 128)).astype(np.float16)
+    q = rng.standard_normal((1, 1, 128))
+    k[0, 0] = (q[0, 0] * 0.8).astype(np.float16)  # a large score for token 0
+    ref = O.attend(q, k.astype(np.float64), v.astype(np.float64), 0.3)
+    errs = []
+    for ns in (0, 5):
+        c = O.OracleCache(_sink_spec(ns, O.ASYM_PER_TOKEN), 1)
+        c.prefill(k, v)
+        errs.append(float(O.row_relative_error(c.decode(q, 0.3), ref).max()))
+    assert errs[1] < errs[0]
