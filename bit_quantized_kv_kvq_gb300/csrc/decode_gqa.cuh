@@ -225,9 +225,22 @@ __global__ void __launch_bounds__(kThreads, 3)
     build_q(nullptr);
 #pragma unroll
     for (int q = 0; q < 4; ++q) qsum_g[q] = 0.0f;
-    for (int c = 0; c < kHeadDim; ++c) {
-      const int q = c / Gk;
-      if (q < 4) qsum_g[q] += qf[g * kHeadDim + c];
+    if (!C::KSYM) {  // symmetric keys have no zero point: the sums are not used
+      // lane t4 of row g sums channels t4, t4 + 4, ... of head g per key group
+      // (groups of 32, 64 or 128 channels), then the row's four lanes combine
+      const int gshift = __ffs(Gk) - 1;
+      for (int c = t4; c < kHeadDim; c += 4) {
+        const float x = qf[g * kHeadDim + c];
+        const int q = c >> gshift;
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq)
+          if (qq == q) qsum_g[qq] += x;
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        qsum_g[q] += __shfl_xor_sync(kFull, qsum_g[q], 1);
+        qsum_g[q] += __shfl_xor_sync(kFull, qsum_g[q], 2);
+      }
     }
   }
   // bias of the current key block for the thread's two heads (2t4, 2t4+1)

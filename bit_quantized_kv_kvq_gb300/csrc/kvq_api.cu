@@ -277,8 +277,10 @@ int k_quant_len(const kvq_config& c, int len) {
 
 // Splits of the sequence: every (stream, split) is one CTA of equal work.
 // With `slots` CTAs resident on the GPU at once, the time of a launch is
-// about waves * (rows per CTA + fixed cost), waves = ceil(CTAs / slots); the
-// split count minimizing it balances wave quantization against short CTAs.
+// about waves * (rows per CTA + fixed cost), waves = ceil(CTAs / slots), plus
+// the merge of a stream's partials by its last CTA (one round of loads per
+// 16 partials); the split count minimizing it balances wave quantization
+// against short CTAs and long merges.
 void plan_splits(const kvq_cache* h, int len, int slots, int* splits, int* tiles_per_split) {
   const int ntiles = (len + kvq::kTile - 1) / kvq::kTile;
   if (h->splits_override > 0) {
@@ -300,7 +302,8 @@ void plan_splits(const kvq_cache* h, int len, int slots, int* splits, int* tiles
     if (s2 != s) continue;  // same shape as a smaller s
     const int64_t ctas = n * s2;
     const int64_t waves = (ctas + slots - 1) / slots;
-    const double t = (double)waves * ((double)tps * kvq::kTile + fixed_rows);
+    const double merge_rows = s2 > 1 ? 48.0 * (double)((s2 + 15) / 16) : 0.0;
+    const double t = (double)waves * ((double)tps * kvq::kTile + fixed_rows) + merge_rows;
     if (t < best * 0.999) {
       best = t;
       best_s = s2;
