@@ -76,6 +76,8 @@ _SIGNATURES = {
     "kvq_decode_attention": [_P, _I, _P, _I, ctypes.c_float, _P, _I, _P, ctypes.c_size_t, _P],
     "kvq_decode_attention_static": [_P, _I, _P, _I, ctypes.c_float, _P, _I, _P],
     "kvq_cache_set_decode_splits": [_P, _I],
+    "kvq_decode_step": [_P, ctypes.POINTER(_P), ctypes.POINTER(_P), ctypes.POINTER(_P), _I, ctypes.c_float,
+                        ctypes.POINTER(_P), _I, _P, ctypes.c_size_t, _P, _P],
     "kvq_cache_get_layout": [_P, _I, ctypes.POINTER(Layout)],
     "kvq_cache_length": [_P, _I, ctypes.POINTER(_I)],
     "kvq_cache_status": [_P, _P, ctypes.POINTER(ctypes.c_uint32)],
@@ -255,6 +257,26 @@ class QuantizedKVCache:
                                                 ctypes.c_void_p(out.data_ptr()), code,
                                                 _stream_ptr(stream)))
         return out
+
+    def decode_step(self, qs, k1s, v1s, softmax_scale, outs, workspace=None, stream=None, aux_stream=None):
+        """Append one token and decode on every layer (kvq_decode_step): qs,
+        k1s, v1s, outs are per-layer tensors; with aux_stream the appends run
+        there, overlapping the decodes of earlier layers."""
+        c = self.cfg
+        nl = c.num_layers
+        if not (len(qs) == len(k1s) == len(v1s) == len(outs) == nl):
+            raise ValueError("one q, k1, v1 and out per layer")
+        hq = qs[0].shape[1]
+        for l in range(nl):
+            _check_half(qs[l], (c.batch, hq, c.head_dim), "q")
+            _check_half(k1s[l], (c.batch, c.num_kv_heads, c.head_dim), "k1")
+            _check_half(v1s[l], (c.batch, c.num_kv_heads, c.head_dim), "v1")
+        code = {torch.float32: F32, torch.float16: F16}[outs[0].dtype]
+        ws = self.workspace(hq) if workspace is None else workspace
+        arr = lambda ts: (_P * nl)(*[t.data_ptr() for t in ts])
+        check(lib().kvq_decode_step(self.handle, arr(qs), arr(k1s), arr(v1s), hq, float(softmax_scale), arr(outs),
+                                    code, ctypes.c_void_p(ws.data_ptr()), ws.numel(), _stream_ptr(stream),
+                                    ctypes.c_void_p(aux_stream.cuda_stream) if aux_stream is not None else None))
 
     # -- inspection ---------------------------------------------------------
     def set_decode_splits(self, splits):

@@ -199,6 +199,12 @@ struct kvq_cache {
   int splits_override = 0;
   int sm_count = 0;
   int device = 0;  // device that holds the buffer; launches need it current
+  std::vector<cudaEvent_t> step_events;  // kvq_decode_step: one per layer + 1, made on first use
+
+  ~kvq_cache() {
+    for (cudaEvent_t e : step_events)
+      if (e) cudaEventDestroy(e);
+  }
 };
 
 namespace {
@@ -575,6 +581,53 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
   a.part_ml = a.part_o + rows * splits * kvq::kHeadDim;
   e = kvq::launch_decode(L, a, st);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+  return KVQ_OK;
+}
+
+kvq_status kvq_decode_step(kvq_cache* h, const void* const* q, const void* const* k1, const void* const* v1,
+                           int32_t num_q_heads, float softmax_scale, void* const* out, int32_t out_dtype,
+                           void* workspace, size_t ws_bytes, void* stream, void* aux_stream) {
+  if (!h) return fail(KVQ_ERR_INVALID_ARG, "cache handle is NULL");
+  kvq_status s = check_device(h);
+  if (s != KVQ_OK) return s;
+  if (!q || !k1 || !v1 || !out) return fail(KVQ_ERR_INVALID_ARG, "q, k1, v1 and out must not be NULL");
+  const int nl = h->cfg.num_layers;
+  for (int l = 0; l < nl; ++l) {  // refuse the whole step before enqueuing any of it
+    if (!q[l] || !k1[l] || !v1[l] || !out[l])
+      return fail(KVQ_ERR_INVALID_ARG, "layer %d: q, k1, v1 and out must not be NULL", l);
+    if (h->len[l] >= h->cfg.max_seq) return fail(KVQ_ERR_CAPACITY, "layer %d is full (%d tokens)", l, h->len[l]);
+  }
+  size_t need = 0;
+  s = kvq_decode_workspace_bytes(h, num_q_heads, &need);
+  if (s != KVQ_OK) return s;
+  if (ws_bytes < need) return fail(KVQ_ERR_BUFFER_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  cudaStream_t main_st = static_cast<cudaStream_t>(stream);
+  cudaStream_t aux = static_cast<cudaStream_t>(aux_stream);
+  if (aux && aux != main_st && h->step_events.empty()) {
+    h->step_events.assign(nl + 1, nullptr);
+    for (auto& e : h->step_events) {
+      const cudaError_t ce = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+      if (ce != cudaSuccess) return cuda_fail(ce, "cudaEventCreateWithFlags");
+    }
+  }
+  const bool two = aux && aux != main_st;
+  if (two) {  // the step's appends start after everything already on `stream`
+    cudaError_t ce = cudaEventRecord(h->step_events[nl], main_st);
+    if (ce == cudaSuccess) ce = cudaStreamWaitEvent(aux, h->step_events[nl], 0);
+    if (ce != cudaSuccess) return cuda_fail(ce, "step ordering");
+  }
+  for (int l = 0; l < nl; ++l) {
+    s = kvq_append_quantize(h, l, k1[l], v1[l], two ? aux : main_st);
+    if (s != KVQ_OK) return s;
+    if (two) {  // layer l's decode waits for layer l's append only
+      cudaError_t ce = cudaEventRecord(h->step_events[l], aux);
+      if (ce == cudaSuccess) ce = cudaStreamWaitEvent(main_st, h->step_events[l], 0);
+      if (ce != cudaSuccess) return cuda_fail(ce, "step ordering");
+    }
+    s = kvq_decode_attention(h, l, q[l], num_q_heads, softmax_scale, out[l], out_dtype, workspace, ws_bytes,
+                             main_st);
+    if (s != KVQ_OK) return s;
+  }
   return KVQ_OK;
 }
 

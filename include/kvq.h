@@ -258,6 +258,22 @@ KVQ_API kvq_status kvq_decode_attention_static(kvq_cache* cache, int32_t layer, 
                                                int32_t num_q_heads, float softmax_scale,
                                                void* out, int32_t out_dtype, void* stream);
 
+/* One decode step of every layer: for each layer l, the append of (k1[l],
+ * v1[l]) and then the decode of q[l] into out[l], as kvq_append_quantize and
+ * kvq_decode_attention (arrays of num_layers device pointers; one workspace
+ * serves every layer's decode, in order on `stream`). With an `aux_stream`
+ * (other than `stream`) the appends run there and layer l's decode waits
+ * only for layer l's append, so the appends of later layers overlap the
+ * decodes of earlier ones (the pages run quantization and attention on
+ * separate streams: [NIAH-q8_0] §4.3); the appends start after everything
+ * already enqueued on `stream`, and the decodes, on `stream`, end the step.
+ * With aux_stream NULL everything runs on `stream` in order. Argument and
+ * capacity errors of any layer are found before anything is enqueued. */
+KVQ_API kvq_status kvq_decode_step(kvq_cache* cache, const void* const* q, const void* const* k1,
+                                   const void* const* v1, int32_t num_q_heads, float softmax_scale,
+                                   void* const* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
+                                   void* stream, void* aux_stream);
+
 /* Forces the number of sequence splits of later decode calls (0 = automatic):
  * for the stream-K decode the number of persistent CTAs (at most one per SM),
  * otherwise the splits per stream. Results agree for every count up to
