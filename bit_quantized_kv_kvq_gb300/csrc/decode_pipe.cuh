@@ -227,6 +227,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
       if (KB != 3) prefetch_map(&maps.k);
       if (VB != 3) prefetch_map(&maps.v);
+      // the query rows of this CTA's streams into L2 while the ring fills
+      const int Hkv = L.num_kv_heads;
+      for (int n = (int)(cA / a.cps); n <= (int)((cB - 1) / a.cps); ++n) {
+        const int b = n / Hkv, kvh = n - b * Hkv;
+        const __half* qr = a.q + ((int64_t)b * a.num_q_heads + (int64_t)kvh * H) * kHeadDim;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(qr), "r"((uint32_t)(H * kHeadDim * 2))
+                     : "memory");
+      }
     }
     for (int u = warp; u < a.ns && u < n_units; u += kCons) {
       const long long ci = cA + u / a.U;
