@@ -85,14 +85,23 @@ bool decode_pipe_supported(const LayerDev& L, int gqa) {
   }
 }
 
-// Partition of the key blocks of all streams over `ctas` CTAs: CTA c takes
-// blocks [c N / P, (c + 1) N / P). A stream of cps blocks meets at most
+// Partition of the key blocks of all streams over `ctas` CTAs. Each stream
+// of cps blocks is followed by `vex` empty places worth the cost of a stream
+// switch (finishing a stream, loading the next query, its first rebuild),
+// and the virtual space of streams * (cps + vex) places is cut evenly: CTA c
+// takes the blocks in [c V / P, (c + 1) V / P). A stream meets at most
 // ceil(P / streams) + 1 CTAs, which bounds the partial rows per stream.
+// Measured on 152 SMs: with 32 streams of 257 blocks of 128 tokens, a switch
+// weighed as 640 tokens brings the slowest CTAs (those crossing a stream
+// boundary) in: 76.3 -> 72.4 us; with 8 streams of 2049 blocks of 64 tokens
+// any weight was slower (84.0 -> 86.0 us), so fewer than 16 streams get none.
 PipePlan plan_decode_pipe(const LayerDev& L, int len, int gqa, int sm_count, int ctas_override) {
   PipePlan p;
   const int T = L.k.group;
   p.cps = (len + T - 1) / T;
   p.n_chunks = (long long)L.n_streams * p.cps;
+  p.vex = L.n_streams >= 16 ? (640 + T - 1) / T : 0;
+  p.n_virtual = (long long)L.n_streams * (p.cps + p.vex);
   int P = sm_count > 0 ? sm_count : 1;
   if (ctas_override > 0 && ctas_override < P) P = ctas_override;
   if ((long long)P > p.n_chunks) P = (int)p.n_chunks;
@@ -126,6 +135,8 @@ cudaError_t launch_decode_pipe(const LayerDev& L, const DecodeArgs& d, const Pip
   a.T = L.k.group;
   a.cps = p.cps;
   a.n_chunks = p.n_chunks;
+  a.vex = p.vex;
+  a.n_virtual = p.n_virtual;
   a.P = p.ctas;
   a.jmax = p.jmax;
   a.kout = L.outliers;

@@ -74,6 +74,8 @@ struct Args {
   int U;                // units per chunk
   int cps;              // chunks per stream
   long long n_chunks;   // chunks of all streams
+  int vex;              // virtual chunks after each stream's blocks (the cost of a stream switch)
+  long long n_virtual;  // n_streams * (cps + vex): the space the CTAs split evenly
   int P;                // CTAs
   int jmax;             // partial rows per stream
   int kout;             // outliers per row
@@ -144,8 +146,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, t4 = lane & 3;
   const int H = a.H;
-  const long long cA = (long long)blockIdx.x * a.n_chunks / a.P;
-  const long long cB = (long long)(blockIdx.x + 1) * a.n_chunks / a.P;
+  // Even split of the virtual chunk space (each stream's blocks followed by
+  // vex empty places), mapped back to real chunks: a CTA whose range crosses
+  // a stream boundary takes fewer blocks, paying for the switch.
+  auto real_of = [&](long long v) {
+    const long long n = v / (a.cps + a.vex), r = v - n * (a.cps + a.vex);
+    return n * a.cps + (r < a.cps ? r : a.cps);
+  };
+  const long long cA = real_of((long long)blockIdx.x * a.n_virtual / a.P);
+  const long long cB = real_of((long long)(blockIdx.x + 1) * a.n_virtual / a.P);
 
   unsigned char* ring = smem;
   unsigned char* wbase = smem + a.ring_bytes;
@@ -808,8 +817,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     };
 
-    // CTA that holds global chunk x
-    auto owner_of = [&](long long x) { return (int)(((x + 1) * a.P - 1) / a.n_chunks); };
+    // CTA that holds global chunk x (through its place in the virtual space)
+    auto owner_of = [&](long long x) {
+      const long long n = x / a.cps, vx = n * (a.cps + a.vex) + (x - n * a.cps);
+      return (int)(((vx + 1) * a.P - 1) / a.n_virtual);
+    };
 
     // Finalizes stream n from accumulator slot `so`: output, or this CTA's
     // partial and, from the last CTA of the stream, the merge of all partials.
@@ -1069,10 +1081,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = ctl[8 + mi];
     const int Hkv = L.num_kv_heads;
     const int b = n / Hkv, kvh = n - b * Hkv;
-    const int P = a.P;
-    const long long N = a.n_chunks;
-    const int cf = (int)((((long long)n * a.cps + 1) * P - 1) / N);
-    const int cl = (int)((((long long)(n + 1) * a.cps) * P - 1) / N);
+    const long long va = (long long)n * (a.cps + a.vex), vb = va + a.cps - 1;  // the stream's first, last block
+    const int cf = (int)(((va + 1) * a.P - 1) / a.n_virtual);
+    const int cl = (int)(((vb + 1) * a.P - 1) / a.n_virtual);
     const int K = cl - cf + 1;
     const float* prn = a.part + (int64_t)n * a.jmax * H * kPartRow;
     for (int h = warp; h < H; h += kCons) {

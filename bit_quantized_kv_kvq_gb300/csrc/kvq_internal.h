@@ -99,6 +99,8 @@ struct PipePlan {
   int jmax;             // partial rows per stream
   int cps;              // key blocks per stream
   long long n_chunks;   // key blocks of all streams
+  int vex;              // empty virtual blocks after each stream (stream-switch cost)
+  long long n_virtual;  // streams * (cps + vex)
   size_t ws_bytes;      // workspace: partials
 };
 bool decode_pipe_supported(const LayerDev& L, int gqa);
