@@ -204,7 +204,7 @@ class Model:
         self.cache = kvq.QuantizedKVCache(wl.num_layers, wl.batch, wl.num_kv_heads, wl.head_dim,
                                           self.S + max_steps, wl.k_bits, wl.v_bits, wl.k_mode,
                                           wl.v_mode, wl.k_group, wl.v_group, wl.outliers_per_row,
-                                          device=device)
+                                          device=device, codebook=wl.codebook)
         self.src = [LayerSource(wl, l, device=device, seed=seed) for l in range(wl.num_layers)]
         self.ws = self.cache.workspace(wl.num_q_heads)
         self.scale = 1.0 / math.sqrt(wl.head_dim)
@@ -428,7 +428,7 @@ def e2e_error(wl, model, device):
 
 def codec_name(bits, mode, group):
     kind = {0: "sym int%d per-token G=%d", 1: "asym %d-bit per-token G=%d",
-            2: "asym %d-bit per-channel T=%d"}[mode]
+            2: "asym %d-bit per-channel T=%d", 3: "codebook %d-bit per-token G=%d"}[mode]
     return kind % (bits, group)
 
 
@@ -502,7 +502,7 @@ def oracle_sample(wl, n_streams, seed):
     k, v = src.kv(wl.seq_len, batch=1)
     n_streams = min(n_streams, wl.num_kv_heads)
     spec = O.CodecSpec(wl.head_dim, wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group,
-                       wl.v_group, wl.outliers_per_row)
+                       wl.v_group, wl.outliers_per_row, 0, wl.codebook)
     oc = O.OracleCache(spec, n_streams)
     t = time.perf_counter()
     oc.prefill(k[0, :n_streams].numpy(), v[0, :n_streams].numpy())
@@ -589,7 +589,7 @@ def profile_case(args, wl):
     S = wl.seq_len
     cache = kvq.QuantizedKVCache(1, wl.batch, wl.num_kv_heads, wl.head_dim, S + 1, wl.k_bits,
                                  wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group, wl.v_group,
-                                 wl.outliers_per_row, device=device)
+                                 wl.outliers_per_row, device=device, codebook=wl.codebook)
     src = LayerSource(wl, 0, device=device)
     k, v = src.kv(S)
     q, k1, v1 = src.step(0)

@@ -13,16 +13,23 @@ import os
 
 import torch
 
+from . import workloads as _W
+
 __all__ = [
     "KVQError", "QuantizedKVCache", "lib", "library_path",
-    "SYM_PER_TOKEN", "ASYM_PER_TOKEN", "ASYM_PER_CHANNEL", "F32", "F16",
+    "SYM_PER_TOKEN", "ASYM_PER_TOKEN", "ASYM_PER_CHANNEL", "CODEBOOK_PER_TOKEN", "F32", "F16",
+    "E2M1_LEVELS",
 ]
 
 SYM_PER_TOKEN = 0
 ASYM_PER_TOKEN = 1
 ASYM_PER_CHANNEL = 2
+CODEBOOK_PER_TOKEN = 3
 F32 = 0
 F16 = 1
+
+# The 4-bit minifloat `1 sign | 2 exponent | 1 mantissa` as codebook levels.
+E2M1_LEVELS = _W.E2M1
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 library_path = os.path.join(_HERE, "libkvq.so")
@@ -43,7 +50,8 @@ class KVQError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_layers", "batch", "num_kv_heads", "head_dim", "max_seq", "k_bits", "v_bits",
-        "k_mode", "v_mode", "k_group", "v_group", "outliers_per_row", "sink_tokens")]
+        "k_mode", "v_mode", "k_group", "v_group", "outliers_per_row")] + [
+        ("codebook", ctypes.c_uint16 * 16), ("sink_tokens", ctypes.c_int32)]
 
 
 class Layout(ctypes.Structure):
@@ -149,9 +157,17 @@ def _stream_ptr(stream):
 
 
 def make_config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits, k_mode,
-                v_mode, k_group, v_group, outliers_per_row=0, sink_tokens=0):
+                v_mode, k_group, v_group, outliers_per_row=0, sink_tokens=0, codebook=None):
+    """codebook: 16 levels (floats, stored as fp16) for CODEBOOK_PER_TOKEN tensors."""
+    cb = (ctypes.c_uint16 * 16)()
+    if codebook is not None:
+        bits = torch.tensor([float(x) for x in codebook], dtype=torch.float16).view(torch.int16)
+        if bits.numel() != 16:
+            raise ValueError("a codebook has 16 levels")
+        for i, b in enumerate(bits.tolist()):
+            cb[i] = b & 0xFFFF
     return Config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits, k_mode,
-                  v_mode, k_group, v_group, outliers_per_row, sink_tokens)
+                  v_mode, k_group, v_group, outliers_per_row, cb, sink_tokens)
 
 
 def cache_bytes(cfg: Config) -> int:
@@ -175,11 +191,12 @@ class QuantizedKVCache:
 
     def __init__(self, num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits, v_bits,
                  k_mode, v_mode, k_group, v_group, outliers_per_row=0, device=None,
-                 stream=None, layer_bits=None, sink_tokens=0):
+                 stream=None, layer_bits=None, sink_tokens=0, codebook=None):
         """layer_bits: None, or one (k_bits, v_bits) pair per layer overriding
         k_bits / v_bits (kvq_cache_create_per_layer)."""
         self.cfg = make_config(num_layers, batch, num_kv_heads, head_dim, max_seq, k_bits,
-                               v_bits, k_mode, v_mode, k_group, v_group, outliers_per_row, sink_tokens)
+                               v_bits, k_mode, v_mode, k_group, v_group, outliers_per_row, sink_tokens,
+                               codebook)
         self.layer_bits = None
         lb = None
         if layer_bits is not None:

@@ -10,7 +10,7 @@ Split-K partials are workspace traffic, not algorithmic bytes.
 """
 from __future__ import annotations
 
-from .workloads import ASYM_PER_CHANNEL, SYM_PER_TOKEN
+from .workloads import ASYM_PER_CHANNEL, CODEBOOK_PER_TOKEN, SYM_PER_TOKEN
 
 
 def _cpw(bits):
@@ -22,7 +22,8 @@ def row_bytes(bits, head_dim=128):
 
 
 def meta_entry_bytes(mode):
-    return 2 if mode == SYM_PER_TOKEN else 4
+    """fp16 scale (symmetric and codebook groups) or fp16 scale + zero point."""
+    return 2 if mode in (SYM_PER_TOKEN, CODEBOOK_PER_TOKEN) else 4
 
 
 def cache_read_bytes(wl, length):

@@ -155,6 +155,8 @@ cudaError_t launch_decode_pipe(const LayerDev& L, const DecodeArgs& d, const Pip
 bool decode_supported(const LayerDev& L, int gqa) {
   if (gqa != 1 && gqa != 2 && gqa != 4 && gqa != 8) return false;
   const int km = L.k.mode, vm = L.v.mode;
+  if (km == KVQ_CODEBOOK_PER_TOKEN || vm == KVQ_CODEBOOK_PER_TOKEN)
+    return km == KVQ_CODEBOOK_PER_TOKEN && vm == KVQ_CODEBOOK_PER_TOKEN;
   if (km == KVQ_SYM_PER_TOKEN || vm == KVQ_SYM_PER_TOKEN)
     return km == KVQ_SYM_PER_TOKEN && vm == KVQ_SYM_PER_TOKEN;
   return vm == KVQ_ASYM_PER_TOKEN;

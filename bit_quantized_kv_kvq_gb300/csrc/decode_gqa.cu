@@ -8,6 +8,7 @@ bool decode_gqa_supported(const LayerDev& L, int gqa) {
   const TensorDev& k = L.k;
   const TensorDev& v = L.v;
   if (L.outliers > 0) return false;
+  if (k.mode == KVQ_CODEBOOK_PER_TOKEN || v.mode == KVQ_CODEBOOK_PER_TOKEN) return false;
   if ((k.bits == 3) != (v.bits == 3)) return false;  // 3-bit keys and values go together
   if (v.mode == KVQ_ASYM_PER_CHANNEL || v.group < 32) return false;
   if (k.mode != KVQ_ASYM_PER_CHANNEL && k.group < 32) return false;

@@ -34,8 +34,11 @@ struct DecodeCfg {
   static constexpr int WK = PK::kWords, WV = PV::kWords;
   static constexpr int CK = PK::kCpw, CV = PV::kCpw;
   static constexpr bool KCH = KMODE == KVQ_ASYM_PER_CHANNEL;
-  static constexpr bool KSYM = KMODE == KVQ_SYM_PER_TOKEN;
-  static constexpr bool VSYM = VMODE == KVQ_SYM_PER_TOKEN;
+  static constexpr bool KCB = KMODE == KVQ_CODEBOOK_PER_TOKEN;  // codes index the codebook
+  static constexpr bool VCB = VMODE == KVQ_CODEBOOK_PER_TOKEN;
+  // scale-only groups (zero point 0): symmetric integer codes and codebook codes
+  static constexpr bool KSYM = KMODE == KVQ_SYM_PER_TOKEN || KCB;
+  static constexpr bool VSYM = VMODE == KVQ_SYM_PER_TOKEN || VCB;
   static constexpr int KMB = KSYM ? 2 : 4;
   static constexpr int VMB = VSYM ? 2 : 4;
   static constexpr int LPRK = WK > 16 ? 32 : 16;  // lanes per key row
@@ -87,6 +90,8 @@ __global__ void __launch_bounds__(kDecThreads)
   float* oc = pb + G * kTile;                                               // [G][128]
   float* ob = oc + G * kHeadDim;                                            // [G][128]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ob + G * kHeadDim);
+  __shared__ float cbt[16];  // codebook levels (codebook codes only)
+  if ((C::KCB || C::VCB) && tid < 16) cbt[tid] = __half2float(__ushort_as_half(L.codebook[tid]));
 
   const int len = a.length, kq = a.k_quant_len;
   const int ntiles = (len + kTile - 1) / kTile;
@@ -212,7 +217,7 @@ __global__ void __launch_bounds__(kDecThreads)
         for (int h = 0; h < G; ++h) dot[h] = 0.0f;
 #pragma unroll
         for (int k = 0; k < C::CK; ++k) {
-          const float f = code_f<KB, C::KSYM>(w, k);
+          const float f = C::KCB ? cbt[(w >> (4 * k)) & 15u] : code_f<KB, C::KSYM>(w, k);
 #pragma unroll
           for (int h = 0; h < G; ++h) dot[h] += qk[h][k] * f;
         }
@@ -326,7 +331,7 @@ __global__ void __launch_bounds__(kDecThreads)
       }
       float f[C::CV];
 #pragma unroll
-      for (int k = 0; k < C::CV; ++k) f[k] = code_f<VB, C::VSYM>(w, k);
+      for (int k = 0; k < C::CV; ++k) f[k] = C::VCB ? cbt[(w >> (4 * k)) & 15u] : code_f<VB, C::VSYM>(w, k);
 #pragma unroll
       for (int h = 0; h < G; ++h) {
         const float pv = pb[h * kTile + row];
@@ -428,6 +433,8 @@ cudaError_t launch_decode_g(const LayerDev& L, const DecodeArgs& a, cudaStream_t
   const int km = L.k.mode, kb = L.k.bits, vm = L.v.mode, vb = L.v.bits;
   if (km == KVQ_SYM_PER_TOKEN && vm == KVQ_SYM_PER_TOKEN)
     return launch_decode_t<8, KVQ_SYM_PER_TOKEN, 8, KVQ_SYM_PER_TOKEN, G>(L, a, st);
+  if (km == KVQ_CODEBOOK_PER_TOKEN && vm == KVQ_CODEBOOK_PER_TOKEN)
+    return launch_decode_t<4, KVQ_CODEBOOK_PER_TOKEN, 4, KVQ_CODEBOOK_PER_TOKEN, G>(L, a, st);
   if (vm != KVQ_ASYM_PER_TOKEN || km == KVQ_SYM_PER_TOKEN) return cudaErrorNotSupported;
 #define KVQ_V(KB_, KM_)                                                                    \
   switch (vb) {                                                                            \

@@ -6,6 +6,7 @@ namespace kvq {
 bool decode_mha_supported(const LayerDev& L) {
   const TensorDev& k = L.k;
   const TensorDev& v = L.v;
+  if (k.mode == KVQ_CODEBOOK_PER_TOKEN || v.mode == KVQ_CODEBOOK_PER_TOKEN) return false;
   if (k.bits == 3 || v.bits == 3) return false;
   // outliers: 4-bit asymmetric codes only (other pairs use the generic kernel)
   if (L.outliers > 0 && (k.bits != 4 || v.bits != 4 || k.mode == KVQ_SYM_PER_TOKEN)) return false;

@@ -3,6 +3,7 @@
 // dispatch. No device memory is allocated here.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <atomic>
@@ -78,8 +79,10 @@ struct Plan {
 kvq_status check_tensor(const char* name, int bits, int mode, int group, bool is_k) {
   if (bits != 3 && bits != 4 && bits != 8)
     return fail(KVQ_ERR_INVALID_ARG, "%s_bits must be 3, 4 or 8 (got %d)", name, bits);
-  if (mode < KVQ_SYM_PER_TOKEN || mode > KVQ_ASYM_PER_CHANNEL)
+  if (mode < KVQ_SYM_PER_TOKEN || mode > KVQ_CODEBOOK_PER_TOKEN)
     return fail(KVQ_ERR_INVALID_ARG, "%s_mode %d is not a kvq_mode", name, mode);
+  if (mode == KVQ_CODEBOOK_PER_TOKEN && bits != 4)
+    return fail(KVQ_ERR_UNSUPPORTED, "codebook groups are supported at 4 bits only");
   if (mode == KVQ_ASYM_PER_CHANNEL) {
     if (!is_k)
       return fail(KVQ_ERR_UNSUPPORTED, "per-channel grouping is supported for keys only");
@@ -90,6 +93,8 @@ kvq_status check_tensor(const char* name, int bits, int mode, int group, bool is
   }
   if (mode == KVQ_SYM_PER_TOKEN && bits != 8)
     return fail(KVQ_ERR_UNSUPPORTED, "symmetric groups are supported at 8 bits only");
+  if (mode == KVQ_CODEBOOK_PER_TOKEN && group < 16)
+    return fail(KVQ_ERR_UNSUPPORTED, "codebook groups must span at least 16 channels");
   if (group != 16 && group != 32 && group != 64 && group != 128)
     return fail(KVQ_ERR_INVALID_ARG, "%s_group must be 16, 32, 64 or 128 channels (got %d)", name,
                 group);
@@ -118,7 +123,22 @@ kvq_status check_config(const kvq_config* c, const int32_t* layer_bits = nullptr
   kvq_status s = check_tensor("k", c->k_bits, c->k_mode, c->k_group, true);
   if (s != KVQ_OK) return s;
   s = check_tensor("v", c->v_bits, c->v_mode, c->v_group, false);
-  if (s != KVQ_OK || !layer_bits) return s;
+  if (s != KVQ_OK) return s;
+  const bool kcb = c->k_mode == KVQ_CODEBOOK_PER_TOKEN, vcb = c->v_mode == KVQ_CODEBOOK_PER_TOKEN;
+  if (kcb != vcb) return fail(KVQ_ERR_UNSUPPORTED, "codebook codes are supported for keys and values together");
+  if (kcb) {
+    if (c->outliers_per_row != 0) return fail(KVQ_ERR_UNSUPPORTED, "codebook codes take no outliers");
+    float mx = 0.0f;
+    for (int i = 0; i < 16; ++i) {
+      __half_raw hr;
+      hr.x = c->codebook[i];
+      const float f = __half2float(__half(hr));
+      if (!std::isfinite(f)) return fail(KVQ_ERR_INVALID_ARG, "codebook level %d is not finite", i);
+      mx = std::fmax(mx, std::fabs(f));
+    }
+    if (!(mx > 0.0f)) return fail(KVQ_ERR_INVALID_ARG, "the codebook has no nonzero level");
+  }
+  if (!layer_bits) return s;
   for (int l = 0; l < c->num_layers; ++l) {
     s = check_tensor("layer k", layer_bits[2 * l], c->k_mode, c->k_group, true);
     if (s == KVQ_OK) s = check_tensor("layer v", layer_bits[2 * l + 1], c->v_mode, c->v_group, false);
@@ -136,7 +156,7 @@ void plan_tensor(const kvq_config& c, int bits, int cap, bool is_k, int64_t* cur
   const int64_t n = (int64_t)c.batch * c.num_kv_heads;
   const int D = kvq::kHeadDim;
   t->words = words_per_row(bits);
-  t->meta_bytes = mode == KVQ_SYM_PER_TOKEN ? 2 : 4;
+  t->meta_bytes = (mode == KVQ_SYM_PER_TOKEN || mode == KVQ_CODEBOOK_PER_TOKEN) ? 2 : 4;
   auto take = [&](int64_t stream_bytes, int64_t* off, int64_t* sb) {
     *sb = round_up(stream_bytes, 16);
     *off = *cursor;
@@ -260,6 +280,7 @@ kvq::LayerDev layer_dev(const kvq_cache* h, int layer) {
   L.sink_tokens = h->cfg.sink_tokens;
   L.sink_k = h->cfg.sink_tokens ? reinterpret_cast<__half*>(h->base + lp.base + lp.sink_k_off) : nullptr;
   L.sink_v = h->cfg.sink_tokens ? reinterpret_cast<__half*>(h->base + lp.base + lp.sink_v_off) : nullptr;
+  std::memcpy(L.codebook, h->cfg.codebook, sizeof L.codebook);
   return L;
 }
 

@@ -49,6 +49,7 @@ struct LayerDev {
   int sink_tokens;      // fp16 attention-sink tokens per stream (0: none)
   __half* sink_k;       // [n][sink_tokens][D]
   __half* sink_v;       // [n][sink_tokens][D]
+  uint16_t codebook[16];  // fp16 levels of KVQ_CODEBOOK_PER_TOKEN tensors
 };
 
 constexpr int kMaxSinkTokens = 64;
@@ -56,6 +57,12 @@ constexpr int kMaxSinkTokens = 64;
 // Prefill of seq_len tokens: k, v fp16 [n][seq_len][D].
 cudaError_t launch_prefill(const LayerDev& L, const __half* k, const __half* v, int seq_len,
                            cudaStream_t stream);
+
+// Codebook tensors (KVQ_CODEBOOK_PER_TOKEN, keys and values): rows
+// [row0, row0 + rows) of every stream from k, v fp16 [n][in_rows][D] (input
+// row i is coded row row0 + i).
+cudaError_t launch_codebook_rows(const LayerDev& L, const __half* k, const __half* v, int rows, int in_rows,
+                                 int row0, cudaStream_t stream);
 
 // Append of one token at position pos (= length before the call): k1, v1
 // fp16 [n][D].

@@ -402,6 +402,7 @@ cudaError_t launch_append_v(const LayerDev& L, const __half* k1, const __half* v
 
 cudaError_t launch_append(const LayerDev& L, const __half* k1, const __half* v1, int pos,
                           cudaStream_t st) {
+  if (L.k.mode == KVQ_CODEBOOK_PER_TOKEN) return launch_codebook_rows(L, k1, v1, 1, 1, pos, st);
   if (L.k.mode == KVQ_SYM_PER_TOKEN) return launch_append_v<8, KVQ_SYM_PER_TOKEN>(L, k1, v1, pos, st);
   if (L.k.mode == KVQ_ASYM_PER_TOKEN) {
     switch (L.k.bits) {

@@ -1,4 +1,5 @@
-"""The five seeded synthetic workloads, described by shape and codec.
+"""The five seeded synthetic workloads, described by shape and codec, and
+the codebook-codec layer beside them.
 
 Each entry names what it is: the tiny q8_0-style GQA layer, the
 Llama-2-7B-shaped MHA layer (two contexts), the Llama-2-70B-shaped GQA layer
@@ -13,6 +14,7 @@ from dataclasses import dataclass, replace
 SYM_PER_TOKEN = 0
 ASYM_PER_TOKEN = 1
 ASYM_PER_CHANNEL = 2
+CODEBOOK_PER_TOKEN = 3
 
 
 @dataclass(frozen=True)
@@ -34,6 +36,7 @@ class Workload:
     outliers_per_row: int = 0
     decode_steps: int = 1
     dist: str = "normal"  # normal | k_lognormal_channels | k_heavy15 | t3_heavy20
+    codebook: tuple = None  # 16 levels of CODEBOOK_PER_TOKEN tensors
 
     @property
     def gqa(self):
@@ -49,7 +52,12 @@ class Workload:
     def codec_kwargs(self):
         return dict(k_bits=self.k_bits, v_bits=self.v_bits, k_mode=self.k_mode,
                     v_mode=self.v_mode, k_group=self.k_group, v_group=self.v_group,
-                    outliers_per_row=self.outliers_per_row)
+                    outliers_per_row=self.outliers_per_row, codebook=self.codebook)
+
+
+# The 4-bit minifloat `1 sign | 2 exponent | 1 mantissa` as 16 codebook levels,
+# indexed by the code's bits (exponent bias 1, subnormal at exponent 0).
+E2M1 = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0)
 
 
 TINY_Q8 = Workload("tiny-q8_0-gqa8x2-d128-s4096", 0, 1, 1, 8, 2, 128, 4096,
@@ -67,5 +75,12 @@ LLAMA8B_FULL = Workload("8b-32layer-h32x8-s131072-k4v8-64steps", 4, 32, 1, 32, 8
                         4, 8, ASYM_PER_CHANNEL, ASYM_PER_TOKEN, 64, 64, decode_steps=64,
                         dist="k_lognormal_channels")
 
+# Beyond the five: the 8B-shaped layer with 4-bit minifloat codebook codes for
+# keys and values, one fp16 scale per 32 channels.
+LLAMA8B_E2M1 = Workload("8b-layer-h32x8-s131072-e2m1-g32", 5, 1, 1, 32, 8, 128, 131072,
+                        4, 4, CODEBOOK_PER_TOKEN, CODEBOOK_PER_TOKEN, 32, 32, decode_steps=64,
+                        dist="k_lognormal_channels", codebook=E2M1)
+
 ALL = [TINY_Q8, LLAMA7B_8K, LLAMA7B_16K, LLAMA70B_32K, DENSE_SPARSE_128K, LLAMA8B_FULL]
-BY_NAME = {w.name: w for w in ALL}
+EXTRA = [LLAMA8B_E2M1]
+BY_NAME = {w.name: w for w in ALL + EXTRA}

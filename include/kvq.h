@@ -75,13 +75,21 @@ typedef enum kvq_status {
  *                       tokens ([KVQuant] §2.2 item 1, [W4A8-FA3] §2.4); keys
  *                       only. The last (length mod group) keys stay in an fp16
  *                       residual until a whole block can be quantized.
- * In every mode code = clamp(rne((x - z16) / s16)) computed in fp32 from the
- * stored fp16 scale s16 and zero point z16 (z16 = 0 for symmetric groups);
- * a group with s16 == 0 stores code 0 everywhere. */
+ *  KVQ_CODEBOOK_PER_TOKEN  non-uniform 4-bit codes ([KVQuant] §2.2 item 2; the
+ *                       4-bit minifloat of [TurboQuant-3bit] §3.3 is one such
+ *                       codebook): per token, groups of `group` channels; one
+ *                       fp16 scale = absmax / max_i |cb_i|, code = the index i
+ *                       of the level cb_i nearest to x / s16 (fp32, lowest index
+ *                       on ties), x_hat = cb[code] * s16. Keys and values both
+ *                       use it or neither; no outliers.
+ * In the integer modes code = clamp(rne((x - z16) / s16)) computed in fp32
+ * from the stored fp16 scale s16 and zero point z16 (z16 = 0 for symmetric
+ * groups); a group with s16 == 0 stores code 0 everywhere. */
 typedef enum kvq_mode {
   KVQ_SYM_PER_TOKEN = 0,
   KVQ_ASYM_PER_TOKEN = 1,
-  KVQ_ASYM_PER_CHANNEL = 2
+  KVQ_ASYM_PER_CHANNEL = 2,
+  KVQ_CODEBOOK_PER_TOKEN = 3
 } kvq_mode;
 
 typedef enum kvq_dtype { KVQ_F32 = 0, KVQ_F16 = 1 } kvq_dtype;
@@ -100,6 +108,8 @@ typedef struct kvq_config {
   int32_t outliers_per_row; /* 0 = dense only; 1..8 fp16 outliers per (token, head)
                                row, chosen by |x| descending, ties to the lower channel
                                ([KVQuant] §2.2 item 3, §3.3)                             */
+  uint16_t codebook[16];    /* fp16 bit patterns of the 16 levels of KVQ_CODEBOOK_PER_TOKEN
+                               tensors (ignored otherwise); finite, max |level| > 0  */
   int32_t sink_tokens;      /* 0..64: the first sink_tokens tokens of every stream are
                                kept in fp16 for keys and values and take part in
                                attention as they are ("attention sinks", [KVQuant]

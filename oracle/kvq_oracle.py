@@ -40,6 +40,7 @@ import numpy as np
 SYM_PER_TOKEN = 0
 ASYM_PER_TOKEN = 1
 ASYM_PER_CHANNEL = 2
+CODEBOOK_PER_TOKEN = 3
 
 
 # ---------------------------------------------------------------------------
@@ -82,7 +83,8 @@ def packed_cache_bytes(num_layers, batch, num_kv_heads, head_dim, seq_len,
 
     Metadata per group: an fp16 scale for symmetric groups (zero point 0,
     [NIAH-q8_0] §1.2); an fp16 scale and an fp16 zero point for asymmetric
-    groups ([TurboQuant-3bit] §3.1, [W4A8-FA3] §2.4).
+    groups ([TurboQuant-3bit] §3.1, [W4A8-FA3] §2.4); an fp16 scale for
+    codebook groups, whose levels carry their own signs (reading R20).
     """
     streams = num_layers * batch * num_kv_heads
     total = 0
@@ -95,7 +97,7 @@ def packed_cache_bytes(num_layers, batch, num_kv_heads, head_dim, seq_len,
                                 + (seq_len - nq) * head_dim * 2)
             rows = nq
         else:
-            meta = 2 if mode == SYM_PER_TOKEN else 4
+            meta = 2 if mode in (SYM_PER_TOKEN, CODEBOOK_PER_TOKEN) else 4
             total += streams * seq_len * (rowb + (head_dim // group) * meta)
             rows = seq_len
         if outliers_per_row:
@@ -211,6 +213,45 @@ def quantize_sym(x16, bits, mask=None):
     return q.astype(np.int64), s16
 
 
+def e2m1_codebook():
+    """The 4-bit minifloat code `1 sign | 2 exponent | 1 mantissa`
+    ([TurboQuant-3bit] §3.3) as a 16-entry codebook indexed by the code's
+    bits s e1 e0 m. Reading R20: exponent bias 1 with e = 0 subnormal, so the
+    magnitudes are m/2 for e = 0 and 2^(e-1) (1 + m/2) otherwise: 0, 0.5, 1,
+    1.5, 2, 3, 4, 6; the sign bit negates. Every value is exact in fp16."""
+    vals = []
+    for code in range(16):
+        sgn, e, m = code >> 3, (code >> 1) & 3, code & 1
+        v = 2.0 ** (e - 1) * (1 + m / 2) if e else m / 2
+        vals.append(-v if sgn else v)
+    return np.array(vals, np.float16)
+
+
+def quantize_codebook(x16, codebook16):
+    """Codebook (non-uniform) quantizer over groups along the last axis
+    ([KVQuant] §2.2 item 2: levels placed where the values are dense;
+    [TurboQuant-3bit] §3.3 for the minifloat levels). Reading R20: one fp16
+    scale per group, s = absmax / max_i |cb_i| (fp32, stored RNE as fp16);
+    y = x / s16 in fp32 (IEEE divide); the code is the index i with the
+    smallest |y - cb_i| in fp32, the lowest index on ties; a group whose
+    scale is 0 stores code 0 everywhere. x_hat = cb[code] * s16.
+
+    Returns codes (int64, same shape as x16) and s16 (float16, shape[:-1])."""
+    x16 = np.asarray(x16, dtype=np.float16)
+    x = x16.astype(np.float32)
+    cb = np.asarray(codebook16, np.float16).astype(np.float32)
+    cbmax = np.float32(np.abs(cb).max())
+    am = np.abs(x).max(axis=-1)
+    s16 = (am / cbmax).astype(np.float16)
+    s = s16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        y = x / s
+    d = np.abs(y[..., None] - cb)                       # [..., 16] in fp32
+    codes = np.argmin(d, axis=-1)                        # first minimum: lowest index on ties
+    codes = np.where(s > 0, codes, 0)
+    return codes.astype(np.int64), s16
+
+
 # ---------------------------------------------------------------------------
 # Bit packing along a (token, head) row
 # ---------------------------------------------------------------------------
@@ -262,6 +303,7 @@ class CodecSpec:
     v_group: int
     outliers_per_row: int = 0
     sink_tokens: int = 0
+    codebook: tuple = None  # 16 fp16 values for CODEBOOK_PER_TOKEN tensors
 
 
 class TensorState:
@@ -309,13 +351,17 @@ class TensorState:
     out_vals = property(lambda self: self._get("out_vals"))
 
 
-def _quantize_rows_per_token(x16, bits, mode, group, k_out):
+def _quantize_rows_per_token(x16, bits, mode, group, k_out, codebook=None):
     n, r, d = x16.shape
     mask, cols, vals = select_outliers(x16, k_out)
     xg = x16.reshape(n, r, d // group, group)
     mg = mask.reshape(n, r, d // group, group)
     if mode == SYM_PER_TOKEN:
         c, s16 = quantize_sym(xg, bits, mg)
+        z16 = None
+    elif mode == CODEBOOK_PER_TOKEN:
+        assert k_out == 0 and codebook is not None
+        c, s16 = quantize_codebook(xg, codebook)
         z16 = None
     else:
         c, s16, z16 = quantize_asym(xg, bits, mg)
@@ -384,7 +430,7 @@ class OracleCache:
         return TensorState(
             codes=np.zeros((n, 0, d), np.int64),
             scale16=np.zeros(meta_shape, np.float16),
-            zero16=None if mode == SYM_PER_TOKEN else np.zeros(meta_shape, np.float16),
+            zero16=None if mode in (SYM_PER_TOKEN, CODEBOOK_PER_TOKEN) else np.zeros(meta_shape, np.float16),
             out_cols=np.zeros((n, 0, ko), np.int64),
             out_vals=np.zeros((n, 0, ko), np.float16),
             resid=np.zeros((n, 0, d), np.float16) if mode == ASYM_PER_CHANNEL else None)
@@ -400,7 +446,7 @@ class OracleCache:
                 st.add(codes=c, scale16=s16, zero16=z16, out_cols=cols, out_vals=vals)
             st.resid = pend[:, nfull:].copy()
         else:
-            c, s16, z16, cols, vals = _quantize_rows_per_token(x16, bits, mode, group, ko)
+            c, s16, z16, cols, vals = _quantize_rows_per_token(x16, bits, mode, group, ko, self.spec.codebook)
             st.add(codes=c, scale16=s16, zero16=z16, out_cols=cols, out_vals=vals)
 
     # -- the decode-loop steps -------------------------------------------
@@ -438,8 +484,8 @@ class OracleCache:
 
     # -- dequantization (fp64) --------------------------------------------
     def _dequant(self, st, mode, group):
-        """x_hat = z16 + c * s16 (asymmetric) or c * s16 (symmetric), exact
-        in fp64; outlier slots take their stored fp16 value (reading R10);
+        """x_hat = z16 + c * s16 (asymmetric), c * s16 (symmetric) or
+        cb[c] * s16 (codebook), exact in fp64; outlier slots take their stored fp16 value (reading R10);
         fp16 residual keys are used as they are."""
         d = self.spec.head_dim
         c = st.codes.astype(np.float64)
@@ -450,6 +496,8 @@ class OracleCache:
             xh = z + c * s
         else:
             s = np.repeat(st.scale16.astype(np.float64), group, axis=2)
+            if mode == CODEBOOK_PER_TOKEN:  # the code indexes the codebook (reading R20)
+                c = np.asarray(self.spec.codebook, np.float16).astype(np.float64)[st.codes]
             xh = c * s
             if mode == ASYM_PER_TOKEN:
                 xh = np.repeat(st.zero16.astype(np.float64), group, axis=2) + xh

@@ -15,16 +15,19 @@ from oracle import kvq_oracle as O
 ATTN_TOL = 1e-3
 
 
-def spec_of(wl, sink_tokens=0):
+def spec_of(wl, sink_tokens=0, codebook=None):
+    codebook = wl.codebook if codebook is None else codebook
     return O.CodecSpec(wl.head_dim, wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode,
-                       wl.k_group, wl.v_group, wl.outliers_per_row, sink_tokens)
+                       wl.k_group, wl.v_group, wl.outliers_per_row, sink_tokens,
+                       None if codebook is None else tuple(float(x) for x in codebook))
 
 
-def make_gpu_cache(wl, max_seq, num_layers=None, device="cuda", sink_tokens=0):
+def make_gpu_cache(wl, max_seq, num_layers=None, device="cuda", sink_tokens=0, codebook=None):
+    codebook = wl.codebook if codebook is None else codebook
     return kvq.QuantizedKVCache(num_layers or wl.num_layers, wl.batch, wl.num_kv_heads,
                                 wl.head_dim, max_seq, wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode,
                                 wl.k_group, wl.v_group, wl.outliers_per_row, device=device,
-                                sink_tokens=sink_tokens)
+                                sink_tokens=sink_tokens, codebook=codebook)
 
 
 def streams_of(x, wl):
@@ -94,11 +97,11 @@ def oracle_state(oc: O.OracleCache, i):
     if sp.k_mode == O.ASYM_PER_CHANNEL:
         out["k_meta"] = np.stack([oc.k.scale16[i].view(np.uint16), oc.k.zero16[i].view(np.uint16)], -1)
         out["k_resid"] = oc.k.resid[i]
-    elif sp.k_mode == O.SYM_PER_TOKEN:
+    elif sp.k_mode in (O.SYM_PER_TOKEN, O.CODEBOOK_PER_TOKEN):
         out["k_meta"] = oc.k.scale16[i].view(np.uint16)[..., None]
     else:
         out["k_meta"] = np.stack([oc.k.scale16[i].view(np.uint16), oc.k.zero16[i].view(np.uint16)], -1)
-    if sp.v_mode == O.SYM_PER_TOKEN:
+    if sp.v_mode in (O.SYM_PER_TOKEN, O.CODEBOOK_PER_TOKEN):
         out["v_meta"] = oc.v.scale16[i].view(np.uint16)[..., None]
     else:
         out["v_meta"] = np.stack([oc.v.scale16[i].view(np.uint16), oc.v.zero16[i].view(np.uint16)], -1)

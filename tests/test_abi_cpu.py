@@ -53,12 +53,12 @@ def _cfg(**kw):
     return kvq.make_config(**base)
 
 
-@pytest.mark.parametrize("wl", W.ALL, ids=lambda w: w.name)
+@pytest.mark.parametrize("wl", W.ALL + W.EXTRA, ids=lambda w: w.name)
 def test_cache_bytes_cover_the_algorithmic_footprint(lib, wl):
     max_seq = wl.seq_len + wl.decode_steps
     cfg = kvq.make_config(wl.num_layers, wl.batch, wl.num_kv_heads, wl.head_dim, max_seq,
                           wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group, wl.v_group,
-                          wl.outliers_per_row)
+                          wl.outliers_per_row, codebook=wl.codebook)
     got = kvq.cache_bytes(cfg)
     algo = O.packed_cache_bytes(wl.num_layers, wl.batch, wl.num_kv_heads, wl.head_dim, max_seq,
                                 wl.k_bits, wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group,
@@ -75,6 +75,16 @@ BAD = [
     (dict(v_bits=3, v_group=64), 2), (dict(outliers_per_row=9), 1), (dict(k_group=32), 2),
     (dict(max_seq=0), 1), (dict(batch=0), 1), (dict(k_mode=7), 1),
 ]
+_CB = dict(k_mode=kvq.CODEBOOK_PER_TOKEN, v_mode=kvq.CODEBOOK_PER_TOKEN, k_group=32, v_group=32,
+           codebook=kvq.E2M1_LEVELS)
+BAD += [
+    (dict(_CB, v_mode=kvq.ASYM_PER_TOKEN), 2),          # keys and values together only
+    (dict(_CB, k_bits=3, v_bits=3, k_group=128, v_group=128), 2),  # 4-bit codes only
+    (dict(_CB, outliers_per_row=2), 2),                 # no outliers beside codebook codes
+    (dict(_CB, codebook=[0.0] * 16), 1),                # no nonzero level
+    (dict(_CB, codebook=[float("inf")] + [1.0] * 15), 1),
+    (dict(_CB, codebook=[float("nan")] + [1.0] * 15), 1),
+]
 
 
 @pytest.mark.parametrize("kw,status", BAD, ids=[str(b[0]) for b in BAD])
@@ -82,6 +92,17 @@ def test_bad_configs_are_rejected(lib, kw, status):
     n = ctypes.c_size_t()
     assert lib.kvq_cache_bytes(ctypes.byref(_cfg(**kw)), ctypes.byref(n)) == status
     assert lib.kvq_last_error()
+
+
+@pytest.mark.parametrize("group", [16, 32, 64, 128])
+def test_codebook_cache_bytes(lib, group):
+    """A codebook cache holds 4-bit codes and one fp16 scale per group."""
+    cfg = _cfg(**dict(_CB, k_group=group, v_group=group))
+    got = kvq.cache_bytes(cfg)
+    algo = O.packed_cache_bytes(1, 2, 4, 128, 1000, 4, 4, O.CODEBOOK_PER_TOKEN, O.CODEBOOK_PER_TOKEN,
+                                group, group)
+    assert algo == 2 * 2 * 4 * 1000 * (64 + 2 * 128 // group)
+    assert algo <= got <= algo + 2 * 4 * 64 * 600 + 4096, (got, algo)
 
 
 def test_create_rejects_bad_buffers_on_the_host(lib):
@@ -132,3 +153,11 @@ def test_per_layer_code_widths_size_the_cache(lib):
     with pytest.raises(kvq.KVQError) as e:
         nbytes(lib.kvq_cache_bytes_per_layer, bad, arr2)
     assert "layer 1" in str(e.value)
+
+
+def test_package_e2m1_levels_match_the_oracle_bit_fields():
+    """The package's minifloat codebook equals the oracle's, which derives
+    each level from the code's sign, exponent and mantissa bits."""
+    import numpy as np
+    a = np.array(kvq.E2M1_LEVELS, np.float16).view(np.uint16)
+    assert np.array_equal(a, O.e2m1_codebook().view(np.uint16))

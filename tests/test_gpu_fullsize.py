@@ -1,4 +1,4 @@
-"""Parity at the full sizes of the five workloads, in the launch
+"""Parity at the full sizes of the five workloads (and the codebook layer), in the launch
 configuration bench.py times: one prefill of the whole context, one append
 and one decode, on the whole batch. The first and the last (batch, kv-head)
 stream are then checked against the oracle run on those streams' inputs
@@ -19,7 +19,7 @@ from tests import kvq_check as K
 
 pytestmark = pytest.mark.gpu
 
-FULL = [(w.name, w) for w in W.ALL]
+FULL = [(w.name, w) for w in W.ALL + W.EXTRA]
 
 
 @pytest.mark.parametrize("name,wl", FULL, ids=[f[0] for f in FULL])

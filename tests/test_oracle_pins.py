@@ -574,7 +574,7 @@ def test_bench_accounting_matches_oracle_footprint(length):
     """bench.py's byte counts (the package's accounting module) equal the
     oracle's footprint for every workload and ragged lengths."""
     from bit_quantized_kv_kvq_gb300 import accounting as A, workloads as W
-    for wl in W.ALL:
+    for wl in W.ALL + W.EXTRA:
         want = O.packed_cache_bytes(1, wl.batch, wl.num_kv_heads, wl.head_dim, length, wl.k_bits,
                                     wl.v_bits, wl.k_mode, wl.v_mode, wl.k_group, wl.v_group,
                                     wl.outliers_per_row)
@@ -663,3 +663,69 @@ def test_sinks_keep_a_dominant_first_token_exact():
         c.prefill(k, v)
         errs.append(float(O.row_relative_error(c.decode(q, 0.3), ref).max()))
     assert errs[1] < errs[0]
+
+
+# ---------------------------------------------------------------------------
+# Codebook codes: the 4-bit minifloat ([TurboQuant-3bit] §3.3) and NUQ
+# levels ([KVQuant] §2.2 item 2)
+# ---------------------------------------------------------------------------
+
+def test_e2m1_codebook_from_its_bit_fields():
+    """1 sign | 2 exponent | 1 mantissa: the positive half is 0, 0.5, 1, 1.5,
+    2, 3, 4, 6 and the sign bit negates (reading R20: bias 1, subnormal at
+    exponent 0)."""
+    cb = O.e2m1_codebook().astype(np.float64)
+    assert cb[:8].tolist() == [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    assert np.array_equal(cb[8:], -cb[:8])
+    assert cb.dtype == np.float64 and np.array_equal(O.e2m1_codebook().astype(np.float64), cb)
+
+
+def test_codebook_codes_are_nearest_levels_bruteforce():
+    """Every code is the index of the level nearest to x / s16 (exact
+    rationals over all 16 levels), the lowest index on exact ties; the scale
+    is absmax / max |level| rounded to fp16."""
+    from fractions import Fraction
+    rng = np.random.default_rng(101)
+    for cb in (O.e2m1_codebook(), np.sort(rng.standard_normal(16)).astype(np.float16)):
+        x = (rng.standard_normal((40, 32)) * rng.uniform(0.01, 100, (40, 1))).astype(np.float16)
+        codes, s16 = O.quantize_codebook(x, cb)
+        cbmax = max(abs(float(v)) for v in cb)
+        for r in range(x.shape[0]):
+            am = max(abs(float(v)) for v in x[r])
+            assert s16[r] == np.float16(np.float32(am) / np.float32(cbmax))
+            s = Fraction(float(s16[r]))
+            for j in range(x.shape[1]):
+                y = np.float32(x[r, j]) / np.float32(s16[r])  # the quotient the codec rounds
+                dist = [abs(Fraction(float(y)) - Fraction(float(v))) for v in cb]
+                best = min(dist)
+                assert codes[r, j] == dist.index(best), (r, j)
+
+
+def test_codebook_levels_reconstruct_exactly_and_zero_groups():
+    """Values that are levels times the scale come back exactly; a zero group
+    stores scale 0 and code 0."""
+    cb = O.e2m1_codebook()
+    s = np.float16(0.125)
+    idx = np.array([[0, 1, 2, 3, 4, 5, 6, 7, 9, 10, 11, 12, 13, 14, 15, 7]])
+    x = (cb.astype(np.float32)[idx] * np.float32(s)).astype(np.float16)  # max |x| = 6 s
+    codes, s16 = O.quantize_codebook(x, cb)
+    assert s16[0] == s
+    assert np.array_equal(cb[codes].astype(np.float64) * float(s16[0]), x.astype(np.float64))
+    codes, s16 = O.quantize_codebook(np.zeros((1, 32), np.float16), cb)
+    assert s16[0] == 0 and np.all(codes == 0)
+
+
+def test_codebook_cache_dequantizes_through_the_levels():
+    """A cache in codebook mode dequantizes x_hat = cb[code] * s16, so its
+    attention equals attention on those values."""
+    rng = np.random.default_rng(102)
+    cb = tuple(float(v) for v in O.e2m1_codebook())
+    spec = O.CodecSpec(128, 4, 4, O.CODEBOOK_PER_TOKEN, O.CODEBOOK_PER_TOKEN, 32, 32, 0, 0, cb)
+    k = rng.standard_normal((2, 50, 128)).astype(np.float16)
+    v = rng.standard_normal((2, 50, 128)).astype(np.float16)
+    c = O.OracleCache(spec, 2)
+    c.prefill(k, v)
+    kc, ks = O.quantize_codebook(k.reshape(2, 50, 4, 32), np.array(cb, np.float16))
+    want = np.array(cb)[kc] * ks.astype(np.float64)[..., None]
+    assert np.array_equal(c.dequant_k(), want.reshape(2, 50, 128))
+    assert c.k.zero16 is None
