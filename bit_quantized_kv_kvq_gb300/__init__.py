@@ -91,6 +91,7 @@ _SIGNATURES = {
     "kvq_cache_status": [_P, _P, ctypes.POINTER(ctypes.c_uint32)],
     "kvq_selftest_div_levels": [_I, ctypes.c_uint32, ctypes.c_uint32, _P, _P],
     "kvq_selftest_code_rounding": [_I, _I, _I, _I, _P, _P],
+    "kvq_selftest_codebook_quotient": [_P, _P],
     "kvq_selftest_wait_timeout": [_P, _I, _P],
 }
 
@@ -138,6 +139,13 @@ def selftest_code_rounding(method, k_first, k_last, ulps, device="cuda", stream=
     rounding near ties against IEEE division (kvq_selftest.h)."""
     return _selftest_result(lambda r: lib().kvq_selftest_code_rounding(method, k_first, k_last, ulps, r,
                                                                        _stream_ptr(stream)), device)
+
+
+def selftest_codebook_quotient(device="cuda", stream=None):
+    """(mismatches, smallest mismatching (s bits << 16 | x bits) or 2^64 - 1)
+    of the codebook quantizer's division-free quotient against IEEE
+    division over every finite fp16 x and positive finite fp16 s."""
+    return _selftest_result(lambda r: lib().kvq_selftest_codebook_quotient(r, _stream_ptr(stream)), device)
 
 
 def kernel_launches() -> int:

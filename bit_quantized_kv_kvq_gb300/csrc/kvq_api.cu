@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <string>
@@ -137,6 +138,20 @@ kvq_status check_config(const kvq_config* c, const int32_t* layer_bits = nullptr
       mx = std::fmax(mx, std::fabs(f));
     }
     if (!(mx > 0.0f)) return fail(KVQ_ERR_INVALID_ARG, "the codebook has no nonzero level");
+    // distinct levels closer than max|level| / 65536 could tie with a level
+    // that is not next to the quantized value after fp32 rounding; the search
+    // table of the quantizer assumes they do not
+    float lv[16];
+    for (int i = 0; i < 16; ++i) {
+      __half_raw hr;
+      hr.x = c->codebook[i];
+      lv[i] = __half2float(__half(hr));
+    }
+    std::sort(lv, lv + 16);
+    for (int i = 1; i < 16; ++i)
+      if (lv[i] != lv[i - 1] && (double)lv[i] - (double)lv[i - 1] < (double)mx / 65536.0)
+        return fail(KVQ_ERR_UNSUPPORTED, "codebook levels %g and %g are closer than max|level| / 65536",
+                    (double)lv[i - 1], (double)lv[i]);
   }
   if (!layer_bits) return s;
   for (int l = 0; l < c->num_layers; ++l) {
@@ -220,6 +235,8 @@ struct kvq_cache {
   int sm_count = 0;
   int device = 0;  // device that holds the buffer; launches need it current
   std::vector<cudaEvent_t> step_events;  // kvq_decode_step: one per layer + 1, made on first use
+  float cb_thr[16] = {};                 // codebook search table (codebook codes only)
+  uint8_t cb_code[16] = {};
 
   ~kvq_cache() {
     for (cudaEvent_t e : step_events)
@@ -281,6 +298,8 @@ kvq::LayerDev layer_dev(const kvq_cache* h, int layer) {
   L.sink_k = h->cfg.sink_tokens ? reinterpret_cast<__half*>(h->base + lp.base + lp.sink_k_off) : nullptr;
   L.sink_v = h->cfg.sink_tokens ? reinterpret_cast<__half*>(h->base + lp.base + lp.sink_v_off) : nullptr;
   std::memcpy(L.codebook, h->cfg.codebook, sizeof L.codebook);
+  std::memcpy(L.cb_thr, h->cb_thr, sizeof L.cb_thr);
+  std::memcpy(L.cb_code, h->cb_code, sizeof L.cb_code);
   return L;
 }
 
@@ -410,6 +429,7 @@ kvq_status kvq_cache_create_per_layer(const kvq_config* cfg, const int32_t* laye
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   kvq_cache* h = new kvq_cache;
   h->cfg = *cfg;
+  if (cfg->k_mode == KVQ_CODEBOOK_PER_TOKEN) kvq::codebook_search_table(cfg->codebook, h->cb_thr, h->cb_code);
   h->plan = p;
   h->base = static_cast<unsigned char*>(dev_buf);
   h->bytes = bytes;

@@ -50,7 +50,19 @@ struct LayerDev {
   __half* sink_k;       // [n][sink_tokens][D]
   __half* sink_v;       // [n][sink_tokens][D]
   uint16_t codebook[16];  // fp16 levels of KVQ_CODEBOOK_PER_TOKEN tensors
+  // The nearest-level decision as a search: y (= x / s16 in fp32) takes code
+  // cb_code[p], p the number of entries of cb_thr (ascending, +inf padded)
+  // that are <= y. Built on the host by codebook_search_table.
+  float cb_thr[16];
+  uint8_t cb_code[16];
 };
+
+// Builds cb_thr / cb_code from 16 fp16 levels: over the distinct levels in
+// ascending order (equal levels, -0 and +0 among them, share the lowest
+// index), cb_thr[k] is the smallest fp32 y that is coded as level k + 1
+// rather than level k. Requires the distinct levels to be at least
+// max|level| / 65536 apart, which check_config enforces.
+void codebook_search_table(const uint16_t levels[16], float thr[16], uint8_t code[16]);
 
 constexpr int kMaxSinkTokens = 64;
 

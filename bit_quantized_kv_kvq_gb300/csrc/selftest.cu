@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cstdio>
 
+#include "codebook.cuh"
 #include "kvq_internal.h"
 #include "kvq_selftest.h"
 #include "prefill_fast.cuh"
@@ -67,6 +68,22 @@ __global__ void __launch_bounds__(kThreads) code_rounding_kernel(int method, uin
       if (got != want)
         note_mismatch(res, ((unsigned long long)sb << 32) | ((unsigned long long)ki << 8) | (unsigned)(j + ulps));
     }
+  }
+}
+
+// Every (finite fp16 x, positive finite fp16 s): the codebook quantizer's
+// quotient against IEEE division, compared as values (+0 == -0).
+__global__ void __launch_bounds__(kThreads) codebook_quotient_kernel(unsigned long long* res) {
+  const uint64_t n = (uint64_t)0x7BFFu * 0x10000u;  // s bits 0x0001..0x7BFF, x bits 0x0000..0xFFFF
+  const uint64_t stride = (uint64_t)gridDim.x * blockDim.x;
+  for (uint64_t t = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n; t += stride) {
+    const uint32_t sb = 1u + (uint32_t)(t >> 16), xb = (uint32_t)(t & 0xFFFFu);
+    const float x = __half2float(__ushort_as_half((unsigned short)xb));
+    if (!isfinite(x)) continue;
+    const float s = __half2float(__ushort_as_half((unsigned short)sb));
+    const float got = kvq::cb::quotient(x, s, __frcp_rn(s));
+    const float want = __fdiv_rn(x, s);
+    if (!(got == want)) note_mismatch(res, ((unsigned long long)sb << 16) | xb);
   }
 }
 
@@ -150,6 +167,14 @@ KVQ_API kvq_status kvq_selftest_code_rounding(int32_t method, int32_t k_first, i
   code_rounding_kernel<<<kBlocks, kThreads, 0, st>>>(method, s_first, s_count, k_first, k_last - k_first + 1, ulps,
                                                      static_cast<unsigned long long*>(dev_result));
   return launched("code rounding self-test launch");
+}
+
+KVQ_API kvq_status kvq_selftest_codebook_quotient(void* dev_result, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const kvq_status s = reset_result(dev_result, st);
+  if (s != KVQ_OK) return s;
+  codebook_quotient_kernel<<<kBlocks, kThreads, 0, st>>>(static_cast<unsigned long long*>(dev_result));
+  return launched("codebook quotient self-test launch");
 }
 
 KVQ_API kvq_status kvq_selftest_wait_timeout(kvq_cache* cache, int32_t polls, void* stream) {

@@ -59,6 +59,17 @@ KVQ_API kvq_status kvq_selftest_div_levels(int32_t levels, uint32_t a_first, uin
 KVQ_API kvq_status kvq_selftest_code_rounding(int32_t method, int32_t k_first, int32_t k_last,
                                               int32_t ulps, void* dev_result, void* stream);
 
+/* The codebook quantizer's quotients (KVQ_CODEBOOK_PER_TOKEN: the group
+ * scale absmax / max|level| and each value's x / s16, KVQuant page,
+ * cf-1.com/news/2306543, §2.2 item 2), formed as RN(x * RN(1/s)) corrected
+ * once by a fused multiply-add (Markstein's division correction). Compares
+ * them as values (+0 equals -0) with __fdiv_rn(x, s) for every finite fp16
+ * x (bit patterns 0x0000..0xFFFF) and every positive finite fp16 s (bit
+ * patterns 0x0001..0x7BFF): about 2.0e9 pairs. Input key:
+ * (s bits << 16) | x bits.
+ * Errors: KVQ_ERR_INVALID_ARG for a NULL or misaligned dev_result. */
+KVQ_API kvq_status kvq_selftest_codebook_quotient(void* dev_result, void* stream);
+
 /* The kernels' bounded wait, made to give up: one CTA initializes an
  * mbarrier that nothing ever completes and waits on it through the same
  * bounded-poll loop the kernels use, with `polls` polls (1..100000) of at

@@ -84,6 +84,7 @@ BAD += [
     (dict(_CB, codebook=[0.0] * 16), 1),                # no nonzero level
     (dict(_CB, codebook=[float("inf")] + [1.0] * 15), 1),
     (dict(_CB, codebook=[float("nan")] + [1.0] * 15), 1),
+    (dict(_CB, codebook=[0.0, 2.0 ** -20] + [1.0] * 14), 2),  # levels closer than max|level| / 65536
 ]
 
 

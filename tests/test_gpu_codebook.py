@@ -53,6 +53,17 @@ def test_codebook_against_the_oracle(case):
     k, v = k.clone(), v.clone()
     k[0, 1, 3, :group] = 0          # a key group that is all zero stores scale 0 and code 0
     v[1, 0, s - 1, -group:] = 0     # and a value group
+    # a group at scale 1 (absmax = max|level|) holding the midpoints of adjacent
+    # levels and the levels themselves: ties and near-ties of the nearest level
+    lv = sorted(set(np.float16(x).item() for x in levels))
+    cbmax = max(abs(x) for x in lv)
+    mids = [cbmax] + [(a + b) / 2 for a, b in zip(lv, lv[1:])] + lv
+    row = torch.tensor((mids * group)[:group], dtype=torch.float16)
+    k[1, 0, 7, :group] = row
+    if group < 128:
+        v[0, 1, 2, group:2 * group] = row.flip(0)
+    else:
+        v[0, 1, 2, :] = row.flip(0)
     cache = K.make_gpu_cache(wl, s + steps + 1, sink_tokens=ns, codebook=levels)
     cache.prefill(0, k.cuda(), v.cuda())
     oc = O.OracleCache(K.spec_of(wl, ns, levels), wl.batch * wl.num_kv_heads)

@@ -47,6 +47,14 @@ def test_bracketed_codes_near_ties():
     assert (mism, first) == (0, NONE), "%d mismatches, first key %#x" % (mism, first)
 
 
+def test_codebook_quotient_is_ieee_for_every_fp16_pair():
+    """The codebook quantizer's x / s without a division (RN(x RN(1/s))
+    corrected once by an fma) equals __fdiv_rn(x, s) for every finite fp16 x
+    and every positive finite fp16 s (2.0e9 pairs)."""
+    mism, first = kvq.selftest_codebook_quotient()
+    assert (mism, first) == (0, NONE), "%d mismatches, first key %#x" % (mism, first)
+
+
 def test_selftest_arguments_are_checked():
     with pytest.raises(kvq.KVQError):
         kvq.selftest_div_levels(5, 0, 10)
