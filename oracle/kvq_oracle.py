@@ -524,6 +524,18 @@ class OracleCache:
             raise ValueError("attention over an empty cache is undefined")
         return attend(q, self.dequant_k(), self.dequant_v(), softmax_scale)
 
+    def prefill_attention(self, q, softmax_scale):
+        """Prefill attention over the quantized cache (reading R22): q is
+        [N][C][g][D], the queries of the last C cached positions of every
+        stream; query i sits at position length - C + i and attends the
+        dequantized tokens 0 .. length - C + i."""
+        q = np.asarray(q, dtype=np.float64)
+        c = q.shape[1]
+        if not 0 < c <= self.length:
+            raise ValueError("the chunk must hold 1 .. length queries")
+        positions = np.arange(self.length - c, self.length)
+        return causal_attend(q, self.dequant_k(), self.dequant_v(), positions, softmax_scale)
+
     # -- packed views in the storage format --------------------------------
     def k_words(self):
         return pack_row_codes(self.k.codes, self.spec.k_bits)
@@ -562,6 +574,20 @@ def attend(q, k_hat, v_hat, softmax_scale):
     p = np.exp(e)
     p /= p.sum(axis=-1, keepdims=True)
     return np.einsum("ngs,nsd->ngd", p, v_hat)
+
+
+def causal_attend(q, k_hat, v_hat, positions, softmax_scale):
+    """Causal attention of a chunk of queries over a cache, in fp64 (reading
+    R22; the prefill of [NIAH-q8_0] §4.2, whose time to first token the
+    chunked queries make up). q: [N][C][g][D]; k_hat, v_hat: [N][S][D];
+    positions: [C] cache positions of the queries. Query i attends tokens
+    0 .. positions[i] (its own token included) exactly as `attend` attends a
+    whole cache. Returns [N][C][g][D]."""
+    q = np.asarray(q, dtype=np.float64)
+    out = np.empty(q.shape, dtype=np.float64)
+    for i, p in enumerate(np.asarray(positions)):
+        out[:, i] = attend(q[:, i], k_hat[:, :int(p) + 1], v_hat[:, :int(p) + 1], softmax_scale)
+    return out
 
 
 def row_relative_error(o, o_ref):

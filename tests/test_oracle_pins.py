@@ -729,3 +729,58 @@ def test_codebook_cache_dequantizes_through_the_levels():
     want = np.array(cb)[kc] * ks.astype(np.float64)[..., None]
     assert np.array_equal(c.dequant_k(), want.reshape(2, 50, 128))
     assert c.k.zero16 is None
+
+
+# ---------------------------------------------------------------------------
+# Prefill attention (causal chunk of queries over the cache, reading R22)
+# ---------------------------------------------------------------------------
+
+def test_causal_attention_of_equal_keys_is_the_running_mean():
+    """With every key equal the weights are uniform: query i returns the mean
+    of the values 0 .. positions[i] (a closed form, no softmax involved)."""
+    rng = np.random.default_rng(11)
+    n, s, d = 2, 9, 8
+    k = np.broadcast_to(rng.standard_normal(d), (n, s, d)).copy()
+    v = rng.standard_normal((n, s, d))
+    q = rng.standard_normal((n, 4, 3, d))
+    pos = np.array([0, 3, 5, 8])
+    o = O.causal_attend(q, k, v, pos, 0.7)
+    run_mean = np.cumsum(v, axis=1) / np.arange(1, s + 1)[None, :, None]
+    for i, p in enumerate(pos):
+        for h in range(3):
+            np.testing.assert_allclose(o[:, i, h], run_mean[:, p], rtol=0, atol=1e-13)
+
+
+def test_causal_attention_hides_later_tokens():
+    """A later token with an overwhelming score changes nothing for queries
+    before it, and takes over the query at its own position."""
+    rng = np.random.default_rng(12)
+    n, s, d = 1, 12, 16
+    k = rng.standard_normal((n, s, d)) * 0.1
+    v = rng.standard_normal((n, s, d))
+    q = rng.standard_normal((n, s, 2, d))
+    k[:, 7] = q[:, 7, 0] * 50.0            # token 7: huge score for head 0 of query 7 onward
+    pos = np.arange(s)
+    o1 = O.causal_attend(q, k, v, pos, 1.0)
+    v2 = v.copy()
+    v2[:, 7] += 100.0
+    o2 = O.causal_attend(q, k, v2, pos, 1.0)
+    np.testing.assert_array_equal(o1[:, :7], o2[:, :7])
+    assert np.abs(o2[:, 7:] - o1[:, 7:]).max() > 1.0
+    np.testing.assert_allclose(o1[:, 7, 0], v[:, 7], rtol=0, atol=1e-9)
+
+
+def test_prefill_attention_last_query_is_the_decode():
+    """The chunk's last query attends the whole cache: the decode of the same
+    cache; a one-query chunk is exactly the decode."""
+    rng = np.random.default_rng(13)
+    spec = O.CodecSpec(128, 4, 4, O.ASYM_PER_CHANNEL, O.ASYM_PER_TOKEN, 64, 32)
+    oc = O.OracleCache(spec, 2)
+    oc.prefill(rng.standard_normal((2, 150, 128)).astype(np.float16),
+               rng.standard_normal((2, 150, 128)).astype(np.float16))
+    q = rng.standard_normal((2, 5, 4, 128))
+    o = oc.prefill_attention(q, 0.1)
+    np.testing.assert_allclose(o[:, -1], oc.decode(q[:, -1], 0.1), rtol=0, atol=1e-12)
+    np.testing.assert_array_equal(oc.prefill_attention(q[:, -1:], 0.1)[:, 0], oc.decode(q[:, -1], 0.1))
+    with pytest.raises(ValueError):
+        oc.prefill_attention(rng.standard_normal((2, 151, 4, 128)), 0.1)
