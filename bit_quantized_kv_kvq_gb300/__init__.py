@@ -92,6 +92,7 @@ _SIGNATURES = {
     "kvq_selftest_div_levels": [_I, ctypes.c_uint32, ctypes.c_uint32, _P, _P],
     "kvq_selftest_code_rounding": [_I, _I, _I, _I, _P, _P],
     "kvq_selftest_codebook_quotient": [_P, _P],
+    "kvq_prefill_attention": [_P, _I, _P, _I, _I, ctypes.c_float, _P, _I, _P],
     "kvq_selftest_wait_timeout": [_P, _I, _P],
 }
 
@@ -281,6 +282,23 @@ class QuantizedKVCache:
                                                 hq, float(softmax_scale),
                                                 ctypes.c_void_p(out.data_ptr()), code,
                                                 _stream_ptr(stream)))
+        return out
+
+    def prefill_attention(self, layer, q, softmax_scale, out=None, out_dtype=torch.float32, stream=None):
+        """Causal attention of the queries of the layer's last q.shape[1]
+        positions over the cache (kvq_prefill_attention): q fp16
+        [B][chunk][H_q][D] -> out [B][chunk][H_q][D]."""
+        c = self.cfg
+        if q.dim() != 4:
+            raise ValueError("q must be [batch][chunk][query heads][head_dim]")
+        chunk, hq = q.shape[1], q.shape[2]
+        _check_half(q, (c.batch, chunk, hq, c.head_dim), "q")
+        if out is None:
+            out = torch.empty((c.batch, chunk, hq, c.head_dim), dtype=out_dtype, device=q.device)
+        code = {torch.float32: F32, torch.float16: F16}[out.dtype]
+        check(lib().kvq_prefill_attention(self.handle, layer, ctypes.c_void_p(q.data_ptr()), chunk, hq,
+                                          float(softmax_scale), ctypes.c_void_p(out.data_ptr()), code,
+                                          _stream_ptr(stream)))
         return out
 
     def decode_step(self, qs, k1s, v1s, softmax_scale, outs, workspace=None, stream=None, aux_stream=None):

@@ -625,6 +625,44 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
   return KVQ_OK;
 }
 
+kvq_status kvq_prefill_attention(kvq_cache* h, int32_t layer, const void* q, int32_t chunk, int32_t num_q_heads,
+                                 float softmax_scale, void* out, int32_t out_dtype, void* stream) {
+  kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  s = check_device(h);
+  if (s != KVQ_OK) return s;
+  if (!q || !out) return fail(KVQ_ERR_INVALID_ARG, "q and out must not be NULL");
+  if (!aligned(q, 16) || !aligned(out, 16)) return fail(KVQ_ERR_INVALID_ARG, "q and out must be 16-byte aligned");
+  if (out_dtype != KVQ_F32 && out_dtype != KVQ_F16)
+    return fail(KVQ_ERR_INVALID_ARG, "out_dtype must be KVQ_F32 or KVQ_F16");
+  const int hkv = h->cfg.num_kv_heads;
+  if (num_q_heads < hkv || num_q_heads % hkv != 0)
+    return fail(KVQ_ERR_INVALID_ARG, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads, hkv);
+  const int len = h->len[layer];
+  if (len == 0) return fail(KVQ_ERR_INVALID_ARG, "layer %d is empty: attention is undefined", layer);
+  if (chunk < 1 || chunk > len)
+    return fail(KVQ_ERR_INVALID_ARG, "chunk %d must be in [1, %d] (the tokens cached)", chunk, len);
+  if ((int64_t)chunk * (num_q_heads / hkv) > ((int64_t)1 << 30))
+    return fail(KVQ_ERR_INVALID_ARG, "chunk * query heads per kv-head is too large");
+  kvq::PrefillAttnArgs a;
+  std::memset(&a, 0, sizeof a);
+  a.q = static_cast<const __half*>(q);
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.num_q_heads = num_q_heads;
+  a.G = num_q_heads / hkv;
+  a.chunk = chunk;
+  a.length = len;
+  a.sink_len = sink_len(h->cfg, len);
+  a.kq = k_quant_len(h->cfg, coded_len(h->cfg, len));
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  const kvq::LayerDev L = layer_dev(h, layer);
+  const cudaError_t e = kvq::launch_prefill_attention(L, a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+  kvq::count_launches(1);
+  return KVQ_OK;
+}
+
 kvq_status kvq_decode_step(kvq_cache* h, const void* const* q, const void* const* k1, const void* const* v1,
                            int32_t num_q_heads, float softmax_scale, void* const* out, int32_t out_dtype,
                            void* workspace, size_t ws_bytes, void* stream, void* aux_stream) {

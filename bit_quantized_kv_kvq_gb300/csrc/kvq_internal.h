@@ -66,6 +66,21 @@ void codebook_search_table(const uint16_t levels[16], float thr[16], uint8_t cod
 
 constexpr int kMaxSinkTokens = 64;
 
+// Prefill attention over the cache (the last `chunk` positions' queries).
+struct PrefillAttnArgs {
+  const __half* q;  // [B][chunk][Hq][D]
+  void* out;        // [B][chunk][Hq][D], fp32 or fp16
+  int out_dtype;
+  int num_q_heads;
+  int G;            // query heads per kv-head
+  int chunk;        // queries per stream: positions length - chunk .. length - 1
+  int length;       // cached tokens (sinks included)
+  int sink_len;     // fp16 sink tokens among them
+  int kq;           // per-channel keys: coded rows held as codes (the rest are the fp16 residual)
+  float scale_log2; // softmax scale * log2(e)
+};
+cudaError_t launch_prefill_attention(const LayerDev& L, const PrefillAttnArgs& a, cudaStream_t stream);
+
 // Prefill of seq_len tokens: k, v fp16 [n][seq_len][D].
 cudaError_t launch_prefill(const LayerDev& L, const __half* k, const __half* v, int seq_len,
                            cudaStream_t stream);

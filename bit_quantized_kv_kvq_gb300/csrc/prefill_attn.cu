@@ -1,0 +1,348 @@
+// Prefill attention over the quantized cache: the queries of the last C
+// cached positions of a layer (the chunk just quantized into the cache)
+// attend, causally, the cache as the decode sees it -- fp16 sink tokens,
+// dequantized codes with their outliers, fp16 residual keys (NIAH q8_0
+// page, cf-1.com/news/5482713, §4.2: the prefill's time to first token; the
+// KVQuant page, cf-1.com/news/2306543, §3.4: attention runs on the
+// dequantized cache). Query i sits at position length - C + i and attends
+// tokens 0 .. length - C + i.
+//
+// This is a dense contraction (C x G query rows against every visible token)
+// and runs on the tensor cores as flash attention: per CTA 128 (position,
+// head) rows of one (batch, kv-head) stream, 16 per warp, over key/value
+// tiles of 64 tokens. The CTA dequantizes each tile once into shared memory
+// as fp16 pairs x = hi + lo (about 22 bits, x formed in fp32 from the codes,
+// scales and zero points), so one kernel serves every codec. Then
+//   S = Q (Khi + Klo)^T                 two m16n8k16 products per fragment
+//   O += (Phi + Plo)(Vhi + Vlo), less Plo Vlo     three products
+// with fp32 accumulation and an exact online softmax in log2 units.
+#include <cstdint>
+
+#include "common.cuh"
+#include "kvq_internal.h"
+#include "mma_frag.cuh"
+
+namespace kvq {
+namespace pa {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
+constexpr int kRowsCta = 16 * kWarps;  // (position, head) rows per CTA
+constexpr int kTT = 64;                // tokens per tile
+constexpr int kLd = kHeadDim + 8;      // shared row stride in halves (272 B: ldmatrix rows on distinct banks)
+constexpr size_t kSmemBytes = (size_t)(kRowsCta + 4 * kTT) * kLd * 2;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+// Code of channel c in a packed row of `bits`-bit codes.
+__device__ __forceinline__ uint32_t code_at(const uint32_t* row, int bits, int c) {
+  const int cpw = bits == 3 ? 10 : bits == 4 ? 8 : 4;
+  const int w = c / cpw, k = c - w * cpw;
+  return (__ldg(row + w) >> (bits * k)) & ((1u << bits) - 1u);
+}
+
+// Eight channels c0 .. c0 + 7 of cached token `tok` of stream n, in fp32.
+template <bool IS_K>
+__device__ __forceinline__ void dequant8(const LayerDev& L, int n, int tok, int c0, int length, int sink_len, int kq,
+                                         const float* cbt, float (&x)[8]) {
+  const bool is_k = IS_K;
+  const TensorDev& T = IS_K ? L.k : L.v;
+  const __half* src = nullptr;  // fp16 row (sinks, residual keys)
+  if (tok >= length) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) x[j] = 0.0f;
+    return;
+  }
+  if (tok < sink_len) {
+    src = (is_k ? L.sink_k : L.sink_v) + ((int64_t)n * L.sink_tokens + tok) * kHeadDim + c0;
+  } else if (is_k && T.mode == KVQ_ASYM_PER_CHANNEL && tok - sink_len >= kq) {
+    src = T.resid + (int64_t)n * T.resid_sstride + (int64_t)(tok - sink_len - kq) * kHeadDim + c0;
+  }
+  if (src) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(src));
+    const __half2* h = reinterpret_cast<const __half2*>(&u);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(h[j]);
+      x[2 * j] = f.x;
+      x[2 * j + 1] = f.y;
+    }
+    return;
+  }
+  const int r = tok - sink_len;  // coded row
+  const uint32_t* row = T.codes + (int64_t)n * T.codes_sstride + (int64_t)r * T.words;
+  const unsigned char* meta = T.meta + (int64_t)n * T.meta_sstride;
+  if (T.mode == KVQ_ASYM_PER_CHANNEL) {
+    const __half2* sz = reinterpret_cast<const __half2*>(meta) + (int64_t)(r / T.group) * kHeadDim + c0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float2 f = __half22float2(sz[j]);
+      x[j] = fmaf((float)code_at(row, T.bits, c0 + j), f.x, f.y);
+    }
+  } else {
+    const int gi = (int)((int64_t)r * (kHeadDim / T.group) + c0 / T.group);  // c0 .. c0 + 7 share a group (G >= 16)
+    if (T.mode == KVQ_ASYM_PER_TOKEN) {
+      const float2 f = __half22float2(reinterpret_cast<const __half2*>(meta)[gi]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = fmaf((float)code_at(row, T.bits, c0 + j), f.x, f.y);
+    } else {
+      const float s = __half2float(reinterpret_cast<const __half*>(meta)[gi]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t c = code_at(row, T.bits, c0 + j);
+        const float v = T.mode == KVQ_CODEBOOK_PER_TOKEN ? cbt[c & 15u] : (float)(int)(int8_t)(uint8_t)c;
+        x[j] = v * s;
+      }
+    }
+  }
+  if (L.outliers > 0) {  // every coded row holds exactly `outliers` entries
+    const int64_t e0 = (int64_t)n * T.out_sstride + (int64_t)r * L.outliers;
+    for (int e = 0; e < L.outliers; ++e) {
+      const int cc = (int)(__ldg(T.col + e0 + e) & (kHeadDim - 1)) - c0;
+      if (cc >= 0 && cc < 8) {
+        const float v = __half2float(__ldg(T.val + e0 + e));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j == cc) x[j] = v;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint4 split8(const float (&x)[8], uint4& lo) {
+  uint4 hi;
+  hi.x = tc::split_pair(x[0], x[1], lo.x);
+  hi.y = tc::split_pair(x[2], x[3], lo.y);
+  hi.z = tc::split_pair(x[4], x[5], lo.z);
+  hi.w = tc::split_pair(x[6], x[7], lo.w);
+  return hi;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDev L, const PrefillAttnArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  __half* qs = reinterpret_cast<__half*>(smem);  // [128][kLd]
+  __half* khi = qs + kRowsCta * kLd;              // [64][kLd] each
+  __half* klo = khi + kTT * kLd;
+  __half* vhi = klo + kTT * kLd;
+  __half* vlo = vhi + kTT * kLd;
+  __shared__ float cbt[16];
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int n = blockIdx.y;
+  const int b = n / L.num_kv_heads, kvh = n - b * L.num_kv_heads;
+  const int G = a.G;
+  const int rows_total = a.chunk * G;
+  const int R0 = blockIdx.x * kRowsCta;
+  const int first_pos = a.length - a.chunk;  // position of query 0
+
+  for (int idx = tid; idx < kRowsCta * 16; idx += kThreads) {
+    const int r = idx >> 4, part = idx & 15;
+    const int R = R0 + r;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (R < rows_total) {
+      const int i = R / G, h = R - i * G;
+      v = __ldg(reinterpret_cast<const uint4*>(
+          a.q + (((int64_t)b * a.chunk + i) * a.num_q_heads + kvh * G + h) * kHeadDim + 8 * part));
+    }
+    *reinterpret_cast<uint4*>(qs + r * kLd + 8 * part) = v;
+  }
+  if (tid < 16) cbt[tid] = __half2float(__ushort_as_half(L.codebook[tid]));
+  __syncthreads();
+
+  // query fragments of the warp's 16 rows (A operand), all 128 channels
+  uint32_t qa[8][4];
+  {
+    const uint32_t base = smem_u32(qs + (16 * warp + (lane & 15)) * kLd + 8 * (lane >> 4));
+#pragma unroll
+    for (int kc = 0; kc < 8; ++kc) ldsm_x4(base + 32u * kc, qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3]);
+  }
+  // positions of the thread's rows g and g + 8 (rows past the chunk attend
+  // the whole cache and are not stored)
+  const int Rw = R0 + 16 * warp;
+  auto pos_of = [&](int R) { return R < rows_total ? first_pos + R / G : a.length - 1; };
+  const int pos0 = pos_of(Rw + g), pos1 = pos_of(Rw + g + 8);
+  const int warp_pos_max = Rw < rows_total ? pos_of(min(Rw + 15, rows_total - 1)) : -1;  // -1: no rows
+  const int last_R = min(R0 + kRowsCta, rows_total) - 1;
+  const int n_tiles = (first_pos + last_R / G) / kTT + 1;
+
+  float o[16][4];
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) o[j][e] = 0.0f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
+
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    const int t0 = tile * kTT;
+    __syncthreads();  // the previous tile is consumed
+    // each thread: four (token, 8-channel) units of K, then four of V
+#pragma unroll 1
+    for (int u = tid; u < kTT * 16; u += kThreads) {
+      const int t = u >> 4, c0 = 8 * (u & 15);
+      float x[8];
+      dequant8<true>(L, n, t0 + t, c0, a.length, a.sink_len, a.kq, cbt, x);
+      uint4 lo;
+      const uint4 hi = split8(x, lo);
+      *reinterpret_cast<uint4*>(khi + t * kLd + c0) = hi;
+      *reinterpret_cast<uint4*>(klo + t * kLd + c0) = lo;
+    }
+#pragma unroll 1
+    for (int u = tid; u < kTT * 16; u += kThreads) {
+      const int t = u >> 4, c0 = 8 * (u & 15);
+      float x[8];
+      dequant8<false>(L, n, t0 + t, c0, a.length, a.sink_len, a.kq, cbt, x);
+      uint4 lo;
+      const uint4 hi = split8(x, lo);
+      *reinterpret_cast<uint4*>(vhi + t * kLd + c0) = hi;
+      *reinterpret_cast<uint4*>(vlo + t * kLd + c0) = lo;
+    }
+    __syncthreads();
+    if (t0 > warp_pos_max) continue;  // every token of the tile is after the warp's rows
+
+    // ---- S = Q K^T (n-tile nt: tokens 8 nt .. 8 nt + 7) ----
+    float s[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) s[j][e] = 0.0f;
+    {
+      const int trow = (lane & 7) + ((lane >> 4) << 3), tcol = ((lane >> 3) & 1) * 8;
+      const uint32_t bh = smem_u32(khi + trow * kLd + tcol), bl = smem_u32(klo + trow * kLd + tcol);
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+        for (int np = 0; np < 4; ++np) {
+          const uint32_t off = (uint32_t)(16 * np * kLd + 16 * kc) * 2u;
+          uint32_t b0, b1, b2, b3;
+          ldsm_x4(bh + off, b0, b1, b2, b3);
+          tc::mma(s[2 * np], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b0, b1);
+          tc::mma(s[2 * np + 1], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b2, b3);
+          ldsm_x4(bl + off, b0, b1, b2, b3);
+          tc::mma(s[2 * np], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b0, b1);
+          tc::mma(s[2 * np + 1], qa[kc][0], qa[kc][1], qa[kc][2], qa[kc][3], b2, b3);
+        }
+    }
+
+    // ---- scale, causal mask, online softmax (rows g: e = 0, 1; g + 8: e = 2, 3) ----
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int tok = t0 + 8 * nt + 2 * t4 + (e & 1);
+        const float v = (tok <= (e < 2 ? pos0 : pos1)) ? s[nt][e] * a.scale_log2 : -INFINITY;
+        s[nt][e] = v;
+        if (e < 2)
+          mx0 = fmaxf(mx0, v);
+        else
+          mx1 = fmaxf(mx1, v);
+      }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(tc::kFull, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(tc::kFull, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(tc::kFull, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(tc::kFull, mx1, 2));
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);  // finite: token 0 is in every row's first tile
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    l0 *= al0;
+    l1 *= al1;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      o[j][0] *= al0;
+      o[j][1] *= al0;
+      o[j][2] *= al1;
+      o[j][3] *= al1;
+    }
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      s[nt][0] = exp2f(s[nt][0] - mn0);
+      s[nt][1] = exp2f(s[nt][1] - mn0);
+      s[nt][2] = exp2f(s[nt][2] - mn1);
+      s[nt][3] = exp2f(s[nt][3] - mn1);
+      l0 += s[nt][0] + s[nt][1];
+      l1 += s[nt][2] + s[nt][3];
+    }
+
+    // ---- O += P V (k-chunk kk: tokens 16 kk .. 16 kk + 15) ----
+    {
+      const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8, vcol = (lane >> 4) * 8;
+      const uint32_t vh = smem_u32(vhi + vrow * kLd + vcol), vl = smem_u32(vlo + vrow * kLd + vcol);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) {
+        uint32_t ph[4], pl[4];
+        ph[0] = tc::split_pair(s[2 * kk][0], s[2 * kk][1], pl[0]);
+        ph[1] = tc::split_pair(s[2 * kk][2], s[2 * kk][3], pl[1]);
+        ph[2] = tc::split_pair(s[2 * kk + 1][0], s[2 * kk + 1][1], pl[2]);
+        ph[3] = tc::split_pair(s[2 * kk + 1][2], s[2 * kk + 1][3], pl[3]);
+#pragma unroll
+        for (int nc = 0; nc < 8; ++nc) {
+          const uint32_t off = (uint32_t)(16 * kk * kLd + 16 * nc) * 2u;
+          uint32_t b0, b1, b2, b3, c0, c1, c2, c3;
+          ldsm_x4_t(vh + off, b0, b1, b2, b3);
+          ldsm_x4_t(vl + off, c0, c1, c2, c3);
+          tc::mma(o[2 * nc], ph[0], ph[1], ph[2], ph[3], b0, b1);
+          tc::mma(o[2 * nc + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+          tc::mma(o[2 * nc], ph[0], ph[1], ph[2], ph[3], c0, c1);
+          tc::mma(o[2 * nc + 1], ph[0], ph[1], ph[2], ph[3], c2, c3);
+          tc::mma(o[2 * nc], pl[0], pl[1], pl[2], pl[3], b0, b1);
+          tc::mma(o[2 * nc + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+        }
+      }
+    }
+  }
+
+  // ---- normalise and store rows g and g + 8 ----
+  l0 += __shfl_xor_sync(tc::kFull, l0, 1);
+  l0 += __shfl_xor_sync(tc::kFull, l0, 2);
+  l1 += __shfl_xor_sync(tc::kFull, l1, 1);
+  l1 += __shfl_xor_sync(tc::kFull, l1, 2);
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int R = Rw + g + 8 * half;
+    if (R >= rows_total) continue;
+    const int i = R / G, h = R - i * G;
+    const float il = 1.0f / (half ? l1 : l0);
+    const int64_t base = (((int64_t)b * a.chunk + i) * a.num_q_heads + kvh * G + h) * kHeadDim + 2 * t4;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float v0 = o[j][2 * half] * il, v1 = o[j][2 * half + 1] * il;
+      if (a.out_dtype == KVQ_F32) {
+        *reinterpret_cast<float2*>(reinterpret_cast<float*>(a.out) + base + 8 * j) = make_float2(v0, v1);
+      } else {
+        *reinterpret_cast<__half2*>(reinterpret_cast<__half*>(a.out) + base + 8 * j) = __floats2half2_rn(v0, v1);
+      }
+    }
+  }
+}
+
+}  // namespace
+}  // namespace pa
+
+cudaError_t launch_prefill_attention(const LayerDev& L, const PrefillAttnArgs& a, cudaStream_t st) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(pa::prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)pa::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int rows = a.chunk * a.G;
+  const dim3 grid((rows + pa::kRowsCta - 1) / pa::kRowsCta, L.n_streams);
+  pa::prefill_attn_kernel<<<grid, pa::kThreads, pa::kSmemBytes, st>>>(L, a);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -284,6 +284,27 @@ KVQ_API kvq_status kvq_decode_step(kvq_cache* cache, const void* const* q, const
                                    void* const* out, int32_t out_dtype, void* workspace, size_t ws_bytes,
                                    void* stream, void* aux_stream);
 
+/* Prefill attention over the quantized cache: the queries of the last
+ * `chunk` cached positions of layer `layer` (the chunk whose K/V were just
+ * quantized into the cache, by kvq_prefill_quantize or appends) attend the
+ * cache causally, as the decode reads it (fp16 sinks, codes with their
+ * outliers, fp16 residual keys) -- the prefill whose time to first token the
+ * pages measure ([NIAH-q8_0] §4.2) on the dequantized cache ([KVQuant] §3.4):
+ *   query i (0 <= i < chunk) sits at position p_i = length - chunk + i;
+ *   e_t = softmax_scale * <q_i, k_hat_t> for t = 0 .. p_i, p = softmax(e),
+ *   o_i = sum_t p_t v_hat_t.
+ * q: fp16 [B][chunk][H_q][D] (token-major, as a prefill's queries come);
+ * out: [B][chunk][H_q][D] in out_dtype. Query head h reads KV head
+ * h / (H_q / H_kv); H_q must be a multiple of H_kv. Every codec of the
+ * cache is served. No workspace; one launch, one CTA per 128 (position,
+ * head) rows of a stream. q and out must be 16-byte aligned; the cache's
+ * device must be current.
+ * Errors: KVQ_ERR_INVALID_ARG for an empty layer, chunk outside
+ * [1, length], NULL or misaligned pointers or a bad out_dtype. */
+KVQ_API kvq_status kvq_prefill_attention(kvq_cache* cache, int32_t layer, const void* q, int32_t chunk,
+                                         int32_t num_q_heads, float softmax_scale, void* out,
+                                         int32_t out_dtype, void* stream);
+
 /* Forces the number of sequence splits of later decode calls (0 = automatic):
  * for the stream-K decode the number of persistent CTAs (at most one per SM),
  * otherwise the splits per stream. Results agree for every count up to
