@@ -46,6 +46,7 @@ from bit_quantized_kv_kvq_gb300 import workloads as W  # noqa: E402
 METRIC = "fused dequant decode-attention KV GB/s (% of GB300 HBM peak); quantize GB/s"
 DEFAULT_WORKLOAD = W.LLAMA8B_FULL.name
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ---------------------------------------------------------------------------
@@ -103,6 +104,54 @@ def hbm_peak():
         return v, "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense fp16/bf16 tensor-core peak (TFLOP/s): the measured cuBLAS bf16
+    burst figure (fp16 inputs with fp32 accumulation run at the same rate)."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def prefill_attention_timing(wl, model, device, flush, chunk=1024, reps=3):
+    """kvq_prefill_attention of the queries of layer 0's last `chunk`
+    positions over its whole cache, L2 flushed before each run. Algorithmic
+    flops: 4 D per (query head, query, visible token) (QK^T and PV, 2 D
+    each)."""
+    cache = model.cache
+    S = model.length()
+    chunk = min(chunk, S)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(wl.seed + 77)
+    q = torch.randn((wl.batch, chunk, wl.num_q_heads, wl.head_dim), generator=gen, device=device).half()
+    out = torch.empty(q.shape, dtype=torch.float32, device=device)
+    cache.prefill_attention(0, q, model.scale, out=out)
+    ts = []
+    for i in range(reps):
+        if flush is not None:
+            flush(i)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record()
+        cache.prefill_attention(0, q, model.scale, out=out)
+        a1.record()
+        torch.cuda.synchronize(device)
+        ts.append(a0.elapsed_time(a1))
+    assert cache.status() == 0
+    visible = chunk * (S - chunk) + chunk * (chunk + 1) // 2
+    flops = 4 * wl.head_dim * wl.num_q_heads * wl.batch * visible
+    m = statistics.median(ts)
+    peak, kind = tensor_peak()
+    tf = flops / (m * 1e-3) / 1e12
+    return {"ms": round(m, 3), "chunk": chunk, "context": S, "flops": flops, "tflops": round(tf, 1),
+            "frac": round(tf / peak, 4), "peak": peak, "peak_kind": kind + " (bf16_tflops, dense; of " + kind + ")",
+            "bound": "tensor",
+            "what": "causal attention of the queries of layer 0's last %d positions over its %d cached tokens "
+                    "(kvq_prefill_attention, fp32 out)" % (chunk, S)}
 
 
 def gpu_id(device):
@@ -356,6 +405,7 @@ def run_gpu(args, wl, rank, world, device):
     del k0, v0
     torch.cuda.synchronize(device)
 
+    pattn = prefill_attention_timing(wl, model, device, flush)
     e2e = run_e2e(args, wl, model, st, device)
     err = e2e_error(wl, model, device)
 
@@ -383,6 +433,7 @@ def run_gpu(args, wl, rank, world, device):
         "quantize": {"gbs": round(gbs(b_pre, m_pre), 1), "ms": round(m_pre, 4), "bytes": b_pre,
                      "frac": round(gbs(b_pre, m_pre) / peak, 4), "what": "prefill of one layer"},
         "append_us_per_layer": round(statistics.mean(app_ms) / L * 1e3, 2),
+        "prefill_attention": pattn,
         "two_stream_step": two_stream,
         "roofline": {"kernel": "decode_attention", "bound": "hbm",
                      "achieved": round(gbs(b_launch, launch_ms), 1), "peak": peak,

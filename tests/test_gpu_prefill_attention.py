@@ -99,3 +99,27 @@ def test_prefill_attention_arguments_are_checked():
     with pytest.raises(kvq.KVQError):
         cache.prefill_attention(0, torch.zeros((1, 4, 3, 128), dtype=torch.float16, device="cuda"), 1.0)
     assert cache.status() == 0
+
+
+def test_prefill_attention_full_size_sampled_streams():
+    """One 8B-shaped layer at its full 131072-token context (8 kv-heads, 32
+    query heads, the launch bench.py times with a shorter chunk): the last
+    64 positions' queries, checked on the first and last stream against the
+    oracle run on those streams alone."""
+    wl = replace(W.LLAMA8B_FULL, num_layers=1)
+    S, N = wl.seq_len, wl.batch * wl.num_kv_heads
+    src = LayerSource(wl, 0, device="cuda")
+    k, v = src.kv(S)
+    cache = K.make_gpu_cache(wl, S + 1)
+    cache.prefill(0, k, v)
+    q = torch.randn((1, 64, wl.num_q_heads, 128), generator=torch.Generator().manual_seed(5)).half()
+    o = cache.prefill_attention(0, q.cuda(), 1.0 / math.sqrt(128))
+    torch.cuda.synchronize()
+    assert cache.status() == 0
+    picks = [0, N - 1]
+    oc = O.OracleCache(K.spec_of(wl), len(picks))
+    oc.prefill(K.streams_of(k, wl)[picks], K.streams_of(v, wl)[picks])
+    del k, v
+    ref = oc.prefill_attention(q_streams(q, wl, wl.gqa)[picks], 1.0 / math.sqrt(128))
+    got = q_streams(o.float(), wl, wl.gqa)[picks]
+    K.assert_attention_close(got.reshape(-1, 128), ref.reshape(-1, 128), where="full size")
