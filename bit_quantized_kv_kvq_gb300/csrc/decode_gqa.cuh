@@ -166,19 +166,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const unsigned char* kmeta = L.k.meta + (int64_t)n * L.k.meta_sstride;
   const unsigned char* vmeta = L.v.meta + (int64_t)n * L.v.meta_sstride;
 
-  for (int i = tid; i < 8 * kHeadDim; i += kThreads) {
-    const int h = i >> 7, c = i & 127;
-    qf[i] = h < G ? __half2float(a.q[((int64_t)b * a.num_q_heads + hq0 + h) * kHeadDim + c]) *
-                        a.scale_log2
-                  : 0.0f;
-  }
   uint64_t* wb = bars + warp * kStagesPerWarp;
-  if (lane == 0) {
-    for (int s = 0; s < kStagesPerWarp; ++s) mbar_init(&wb[s], 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-
   auto stage_ptr = [&](int s) { return stages + (size_t)(warp * kStagesPerWarp + s) * C::STAGE; };
   auto issue = [&](int ti, int s) {
     unsigned char* base = stage_ptr(s);
@@ -197,8 +185,21 @@ __global__ void __launch_bounds__(kThreads, 3)
     bulk_g2s(base + C::KC_BYTES + C::VC_BYTES + C::META,
              vmeta + (int64_t)t0 * vgpr * (C::VSYM ? 2 : 4), vmb, &wb[s]);
   };
-  if (lane == 0)
+  // lane 0 of each warp: its barriers and its first copies, before the
+  // query load, so that the two latencies overlap
+  if (lane == 0) {
+    for (int s = 0; s < kStagesPerWarp; ++s) mbar_init(&wb[s], 1);
+    mbar_fence_init();
     for (int s = 0; s < kStagesPerWarp && s < w_count; ++s) issue(s, s);
+  }
+
+  for (int i = tid; i < 8 * kHeadDim; i += kThreads) {
+    const int h = i >> 7, c = i & 127;
+    qf[i] = h < G ? __half2float(a.q[((int64_t)b * a.num_q_heads + hq0 + h) * kHeadDim + c]) *
+                        a.scale_log2
+                  : 0.0f;
+  }
+  __syncthreads();
 
   // ---- query fragments (B operand of QK^T), head = g ---------------------------
   // per-token keys: fixed; per-channel keys: rebuilt per key block with q*s.

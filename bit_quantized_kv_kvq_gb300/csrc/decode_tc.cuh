@@ -159,24 +159,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
   const unsigned char* kmeta = L.k.meta + (int64_t)n * L.k.meta_sstride;
   const unsigned char* vmeta = L.v.meta + (int64_t)n * L.v.meta_sstride;
 
-  for (int i = tid; i < HQ * kHeadDim; i += kThreads) {
-    const int h = i >> 7, c = i & 127;
-    const float v = h < G ? __half2float(a.q[((int64_t)b * a.num_q_heads + hq0 + h) * kHeadDim + c]) *
-                                a.scale_log2
-                          : 0.0f;
-    qf[i] = v;
-    qm[i] = v * __uint_as_float((uint32_t)(127 - key_shift<KB>(c)) << 23);
-  }
-  for (int i = lane; i < 32 * NT * 16; i += 32) frag[i] = 0u;
-  if (OUTL)
-    for (int i = lane; i < HQ * kHeadDim; i += 32) ocr[i] = 0.0f;
   uint64_t* wb = bars + warp * S;
-  if (lane == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&wb[s], 1);
-    mbar_fence_init();
-  }
-  __syncthreads();
-
   auto stage_ptr = [&](int s) { return stages + (size_t)(warp * S + s) * STG; };
   // Staging of tile ti into stage s (one lane issues every copy).
   auto issue = [&](int ti, int s) {
@@ -204,8 +187,26 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
       bulk_g2s(ot + 3 * ob, L.v.val + (int64_t)n * L.v.out_sstride + e0, ob, &wb[s]);
     }
   };
-  if (lane == 0)
+  // lane 0 of each warp: its barriers and its first copies, before the
+  // query load, so that the two latencies overlap
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&wb[s], 1);
+    mbar_fence_init();
     for (int s = 0; s < S && s < w_count; ++s) issue(s, s);
+  }
+
+  for (int i = tid; i < HQ * kHeadDim; i += kThreads) {
+    const int h = i >> 7, c = i & 127;
+    const float v = h < G ? __half2float(a.q[((int64_t)b * a.num_q_heads + hq0 + h) * kHeadDim + c]) *
+                                a.scale_log2
+                          : 0.0f;
+    qf[i] = v;
+    qm[i] = v * __uint_as_float((uint32_t)(127 - key_shift<KB>(c)) << 23);
+  }
+  for (int i = lane; i < 32 * NT * 16; i += 32) frag[i] = 0u;
+  if (OUTL)
+    for (int i = lane; i < HQ * kHeadDim; i += 32) ocr[i] = 0.0f;
+  __syncthreads();
 
   // ---- state ------------------------------------------------------------------
   uint32_t bq[NT][8][2];
