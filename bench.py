@@ -627,7 +627,8 @@ def run_reference(args, wl, rank, world):
 
 def profile_case(args, wl):
     """A short untimed run for profilers: prefill, append and decode of the
-    workload's codec and shape at a reduced batch, args.reps times."""
+    workload's codec and shape at a reduced batch, args.reps times; with
+    --chunk C, then the prefill attention of the last C positions."""
     import dataclasses
     import bit_quantized_kv_kvq_gb300 as kvq
     from bit_quantized_kv_kvq_gb300.synth import LayerSource
@@ -648,6 +649,12 @@ def profile_case(args, wl):
         cache.prefill(0, k, v)
         cache.append(0, k1, v1)
         cache.decode(0, q, 1.0 / math.sqrt(wl.head_dim))
+    if args.chunk:
+        gen = torch.Generator(device=device)
+        gen.manual_seed(wl.seed + 77)
+        qc = torch.randn((wl.batch, min(args.chunk, S + 1), wl.num_q_heads, wl.head_dim), generator=gen,
+                         device=device).half()
+        cache.prefill_attention(0, qc, 1.0 / math.sqrt(wl.head_dim))
     torch.cuda.synchronize(device)
     if cache.status() != 0:
         raise RuntimeError("device status word %#x" % cache.status())
@@ -669,6 +676,8 @@ def main(argv=None):
     ap.add_argument("--batch", type=int, default=0, help="batch of --profile-case (0: workload's)")
     ap.add_argument("--reps", type=int, default=2, help="repetitions of --profile-case")
     ap.add_argument("--seq", type=int, default=0, help="context length of --profile-case (0: workload's)")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="--profile-case: then prefill attention of the last CHUNK positions (0: none)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
