@@ -8,7 +8,8 @@ bool decode_gqa_supported(const LayerDev& L, int gqa) {
   const TensorDev& k = L.k;
   const TensorDev& v = L.v;
   if (L.outliers > 0) return false;
-  if (k.mode == KVQ_CODEBOOK_PER_TOKEN || v.mode == KVQ_CODEBOOK_PER_TOKEN) return false;
+  if (k.mode == KVQ_CODEBOOK_PER_TOKEN || v.mode == KVQ_CODEBOOK_PER_TOKEN)  // 4-bit, groups of 32 .. 128
+    return k.mode == v.mode && k.group >= 32 && v.group >= 32;
   if ((k.bits == 3) != (v.bits == 3)) return false;  // 3-bit keys and values go together
   if (v.mode == KVQ_ASYM_PER_CHANNEL || v.group < 32) return false;
   if (k.mode != KVQ_ASYM_PER_CHANNEL && k.group < 32) return false;
@@ -20,6 +21,8 @@ cudaError_t launch_decode_gqa(const LayerDev& L, const DecodeArgs& a, cudaStream
   const int kb = L.k.bits, vb = L.v.bits, km = L.k.mode;
   if (km == KVQ_SYM_PER_TOKEN)
     return gqa::launch_t<8, KVQ_SYM_PER_TOKEN, 8, KVQ_SYM_PER_TOKEN>(L, a, st);
+  if (km == KVQ_CODEBOOK_PER_TOKEN)
+    return gqa::launch_t<4, KVQ_CODEBOOK_PER_TOKEN, 4, KVQ_CODEBOOK_PER_TOKEN>(L, a, st);
 #define KVQ_GQA(KB_, KM_)                                                          \
   if (kb == KB_ && km == KM_) {                                                    \
     if (vb == 4) return gqa::launch_t<KB_, KM_, 4, KVQ_ASYM_PER_TOKEN>(L, a, st);  \

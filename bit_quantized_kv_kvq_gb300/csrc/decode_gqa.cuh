@@ -74,6 +74,12 @@ struct Cfg {
   static constexpr bool KCH = KMODE == KVQ_ASYM_PER_CHANNEL;
   static constexpr bool KSYM = KMODE == KVQ_SYM_PER_TOKEN;
   static constexpr bool VSYM = VMODE == KVQ_SYM_PER_TOKEN;
+  // codebook codes: a 4-bit code indexes 16 fp16 levels (one table lookup
+  // per pair of codes); like symmetric codes their groups have a scale only
+  static constexpr bool KCB = KMODE == KVQ_CODEBOOK_PER_TOKEN;
+  static constexpr bool VCB = VMODE == KVQ_CODEBOOK_PER_TOKEN;
+  static constexpr bool KSC = KSYM || KCB;  // scale-only key groups
+  static constexpr bool VSC = VSYM || VCB;
   static constexpr int KW = Pack<KB>::kWords, VW = Pack<VB>::kWords;
   static constexpr int KC_BYTES = kRows * KW * 4;
   static constexpr int VC_BYTES = kRows * VW * 4;
@@ -172,18 +178,18 @@ __global__ void __launch_bounds__(kThreads, 3)
     unsigned char* base = stage_ptr(s);
     const int t0 = row_begin + (w_first + ti) * kRows;
     const bool rt = C::KCH && t0 >= kq;
-    const uint32_t kmb = C::KCH ? (uint32_t)(kHeadDim * 4) : (uint32_t)(kRows * kgpr * (C::KSYM ? 2 : 4));
-    const uint32_t vmb = (uint32_t)(kRows * vgpr * (C::VSYM ? 2 : 4));
+    const uint32_t kmb = C::KCH ? (uint32_t)(kHeadDim * 4) : (uint32_t)(kRows * kgpr * (C::KSC ? 2 : 4));
+    const uint32_t vmb = (uint32_t)(kRows * vgpr * (C::VSC ? 2 : 4));
     mbar_arrive_expect_tx(&wb[s], C::VC_BYTES + vmb + (rt ? 0u : C::KC_BYTES + kmb));
     if (!rt) {
       bulk_g2s(base, kcodes + (int64_t)t0 * C::KW, C::KC_BYTES, &wb[s]);
       const unsigned char* ks = C::KCH ? kmeta + (int64_t)(t0 / Gk) * kHeadDim * 4
-                                       : kmeta + (int64_t)t0 * kgpr * (C::KSYM ? 2 : 4);
+                                       : kmeta + (int64_t)t0 * kgpr * (C::KSC ? 2 : 4);
       bulk_g2s(base + C::KC_BYTES + C::VC_BYTES, ks, kmb, &wb[s]);
     }
     bulk_g2s(base + C::KC_BYTES, vcodes + (int64_t)t0 * C::VW, C::VC_BYTES, &wb[s]);
     bulk_g2s(base + C::KC_BYTES + C::VC_BYTES + C::META,
-             vmeta + (int64_t)t0 * vgpr * (C::VSYM ? 2 : 4), vmb, &wb[s]);
+             vmeta + (int64_t)t0 * vgpr * (C::VSC ? 2 : 4), vmb, &wb[s]);
   };
   // lane 0 of each warp: its barriers and its first copies, before the
   // query load, so that the two latencies overlap
@@ -199,6 +205,11 @@ __global__ void __launch_bounds__(kThreads, 3)
                         a.scale_log2
                   : 0.0f;
   }
+  // codebook codes: entry i holds the fp16 pair (level[i & 15], level[i >> 4])
+  __shared__ uint32_t cbl[(C::KCB || C::VCB) ? 256 : 1];
+  if (C::KCB || C::VCB)
+    for (int i = tid; i < 256; i += kThreads)
+      cbl[i] = (uint32_t)L.codebook[i & 15] | ((uint32_t)L.codebook[i >> 4] << 16);
   __syncthreads();
 
   // ---- query fragments (B operand of QK^T), head = g ---------------------------
@@ -226,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     build_q(nullptr);
 #pragma unroll
     for (int q = 0; q < 4; ++q) qsum_g[q] = 0.0f;
-    if (!C::KSYM) {  // symmetric keys have no zero point: the sums are not used
+    if (!C::KSC) {  // scale-only keys have no zero point: the sums are not used
       // lane t4 of row g sums channels t4, t4 + 4, ... of head g per key group
       // (groups of 32, 64 or 128 channels), then the row's four lanes combine
       const int gshift = __ffs(Gk) - 1;
@@ -337,10 +348,17 @@ __global__ void __launch_bounds__(kThreads, 3)
             const uint32_t sel = (uint32_t)(t4 | (t4 << 4) | ((4 + t4) << 8) | ((4 + t4) << 12));
             const uint32_t x0 = __byte_perm(w0.x, w0.y, sel);
             const uint32_t x1 = __byte_perm(w1.x, w1.y, sel);
-            af[0] = hsub2u((x0 & 0x000F000Fu) | kH1024, kH1024);
-            af[2] = hsub2u(((x0 >> 4) & 0x000F000Fu) | kH1024, kH1024);
-            af[1] = hsub2u((x1 & 0x000F000Fu) | kH1024, kH1024);
-            af[3] = hsub2u(((x1 >> 4) & 0x000F000Fu) | kH1024, kH1024);
+            if (C::KCB) {  // the two codes of each half pair index the level-pair table
+              af[0] = cbl[(x0 & 0xFu) | ((x0 >> 12) & 0xF0u)];
+              af[2] = cbl[((x0 >> 4) & 0xFu) | ((x0 >> 16) & 0xF0u)];
+              af[1] = cbl[(x1 & 0xFu) | ((x1 >> 12) & 0xF0u)];
+              af[3] = cbl[((x1 >> 4) & 0xFu) | ((x1 >> 16) & 0xF0u)];
+            } else {
+              af[0] = hsub2u((x0 & 0x000F000Fu) | kH1024, kH1024);
+              af[2] = hsub2u(((x0 >> 4) & 0x000F000Fu) | kH1024, kH1024);
+              af[1] = hsub2u((x1 & 0x000F000Fu) | kH1024, kH1024);
+              af[3] = hsub2u(((x1 >> 4) & 0x000F000Fu) | kH1024, kH1024);
+            }
           } else {
             const int per = gp / 16;
             const int q = kc / per, l = kc - q * per;
@@ -379,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, 3)
           float sA = 0.0f, sB = 0.0f, sC = 0.0f, sD = 0.0f;
           for (int q = 0; q < kgpr; ++q) {
             float s_r0, s_r1, z_r0 = 0.0f, z_r1 = 0.0f;
-            if (C::KSYM) {
+            if (C::KSC) {
               s_r0 = __half2float(reinterpret_cast<const __half*>(km)[r0 * kgpr + q]);
               s_r1 = __half2float(reinterpret_cast<const __half*>(km)[r1 * kgpr + q]);
             } else {
@@ -498,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         bph0[q] = bph1[q] = bpl0[q] = bpl1[q] = 0u;
         if (q < vgpr) {  // warp-uniform
           float sv0, sv1, zv0 = 0.0f, zv1 = 0.0f;
-          if (C::VSYM) {
+          if (C::VSC) {
             sv0 = __half2float(reinterpret_cast<const __half*>(vm)[r0 * vgpr + q]);
             sv1 = __half2float(reinterpret_cast<const __half*>(vm)[r1 * vgpr + q]);
           } else {
@@ -554,10 +572,17 @@ __global__ void __launch_bounds__(kThreads, 3)
           const uint32_t wc = vc_s[(ra + 8) * C::VW + wi], wd = vc_s[(ra + 9) * C::VW + wi];
           const uint32_t sel2 = (uint32_t)(i | (i << 4) | ((4 + i) << 8) | ((4 + i) << 12));
           const uint32_t xab = __byte_perm(wa, wb2, sel2), xcd = __byte_perm(wc, wd, sel2);
-          af[0] = hsub2u((xab & 0x000F000Fu) | kH1024, kH1024);
-          af[1] = hsub2u(((xab >> 4) & 0x000F000Fu) | kH1024, kH1024);
-          af[2] = hsub2u((xcd & 0x000F000Fu) | kH1024, kH1024);
-          af[3] = hsub2u(((xcd >> 4) & 0x000F000Fu) | kH1024, kH1024);
+          if (C::VCB) {
+            af[0] = cbl[(xab & 0xFu) | ((xab >> 12) & 0xF0u)];
+            af[1] = cbl[((xab >> 4) & 0xFu) | ((xab >> 16) & 0xF0u)];
+            af[2] = cbl[(xcd & 0xFu) | ((xcd >> 12) & 0xF0u)];
+            af[3] = cbl[((xcd >> 4) & 0xFu) | ((xcd >> 16) & 0xF0u)];
+          } else {
+            af[0] = hsub2u((xab & 0x000F000Fu) | kH1024, kH1024);
+            af[1] = hsub2u(((xab >> 4) & 0x000F000Fu) | kH1024, kH1024);
+            af[2] = hsub2u((xcd & 0x000F000Fu) | kH1024, kH1024);
+            af[3] = hsub2u(((xcd >> 4) & 0x000F000Fu) | kH1024, kH1024);
+          }
         } else {
           const int u = g >> 1, bb = g & 1;
           const int wi = q * (Gv / 4) + u * (Gv / 16) + l;
