@@ -443,21 +443,13 @@ __device__ __forceinline__ void clear_field(uint32_t (&w)[PB / 4], int i) {
   }
 }
 
-// Word w (ten 3-bit codes, top two bits zero; word 12 holds eight) of a row
-// whose 128 codes sit one per byte in shared memory (16-byte aligned).
-__device__ __forceinline__ uint32_t pack3_word(const unsigned char* row, int w) {
-  const int b0 = 10 * w, base = b0 & ~3;
-  const uint32_t u0 = *reinterpret_cast<const uint32_t*>(row + base);
-  const uint32_t u1 = *reinterpret_cast<const uint32_t*>(row + base + 4);
-  const uint32_t u2 = w < 12 ? *reinterpret_cast<const uint32_t*>(row + base + 8) : 0u;
-  const bool odd = b0 != base;  // the word starts at byte 2 of an aligned group
-  const uint32_t x0 = odd ? __byte_perm(u0, u1, 0x5432u) : u0;
-  const uint32_t x1 = odd ? __byte_perm(u1, u2, 0x5432u) : u1;
-  const uint32_t x2 = odd ? (u2 >> 16) : u2;
-  auto comb4 = [](uint32_t x) {
-    return (x & 0x7u) | ((x >> 5) & 0x38u) | ((x >> 10) & 0x1C0u) | ((x >> 15) & 0xE00u);
-  };
-  return comb4(x0) | (comb4(x1) << 12) | ((x2 & 0x7u) << 24) | (((x2 >> 8) & 0x7u) << 27);
+// Ten-per-word packing in registers. comb4: the four one-byte codes of a
+// word as four 3-bit fields (12 bits). A lane holding the codes of channels
+// c0 .. c0 + k - 1 contributes 3k bits at bit 3 c0 of the row's 3-bit
+// stream; word w of the row is the stream's bits 30 w .. 30 w + 29, taken
+// from at most two neighbouring lanes by shuffles.
+__device__ __forceinline__ uint32_t comb4(uint32_t x) {
+  return (x & 0x7u) | ((x >> 5) & 0x38u) | ((x >> 10) & 0x1C0u) | ((x >> 15) & 0xE00u);
 }
 
 // ---------------------------------------------------------------------------
@@ -629,17 +621,30 @@ __device__ __forceinline__ void rows_warp(const unsigned char* tile, const Tenso
       if (q == 0) write_rowptr(T, n, row0 + lr, kout);
     }
     if (BITS == 3) {
-      // ten codes per word: through this warp's row buffer (one byte per code)
-      unsigned char* rb = rowbuf + rr * kHeadDim;
-      *reinterpret_cast<uint2*>(rb + 8 * c0) = make_uint2(wa0[0], wa0[PB / 4 - 1]);
-      *reinterpret_cast<uint2*>(rb + 8 * c1) = make_uint2(wa1[0], wa1[PB / 4 - 1]);
-      __syncwarp();
+      // ten codes per word: the lane's 16 codes (channels 16 q ..) are 48 bits
+      // at bit 48 q of the row's stream; it writes words q and q + 8
+      const uint32_t* lo = sw ? wa1 : wa0;  // chunk 2q
+      const uint32_t* hi = sw ? wa0 : wa1;  // chunk 2q + 1
+      const uint32_t f0 = comb4(lo[0]), f1 = comb4(lo[PB / 4 - 1]);
+      const uint32_t f2 = comb4(hi[0]), f3 = comb4(hi[PB / 4 - 1]);
+      const uint32_t p_lo = f0 | (f1 << 12) | (f2 << 24), p_hi = (f2 >> 8) | (f3 << 4);
+      const int rbase = lane & ~7;
+      uint32_t word[2];
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const int w = min(q + 8 * k, kWords - 1);
+        const int A = (5 * w) >> 3, oA = 30 * w - 48 * A;  // first source lane, bit offset in it
+        const uint32_t alo = __shfl_sync(kFull, p_lo, rbase + A), ahi = __shfl_sync(kFull, p_hi, rbase + A);
+        const uint32_t blo = __shfl_sync(kFull, p_lo, rbase + min(A + 1, 7));
+        const uint64_t pa = (uint64_t)alo | ((uint64_t)ahi << 32);
+        const uint64_t pb = A + 1 < 8 ? (uint64_t)blo << (48 - oA) : 0ull;
+        word[k] = (uint32_t)((pa >> oA) | pb) & 0x3FFFFFFFu;
+      }
       if (live) {
         uint32_t* rowdst = T.codes + (int64_t)n * T.codes_sstride + (int64_t)(row0 + lr) * kWords;
-        rowdst[q] = pack3_word(rb, q);
-        if (q + 8 < kWords) rowdst[q + 8] = pack3_word(rb, q + 8);
+        rowdst[q] = word[0];
+        if (q + 8 < kWords) rowdst[q + 8] = word[1];
       }
-      __syncwarp();
     } else if (live) {
       uint32_t* rowdst = T.codes + (int64_t)n * T.codes_sstride + (int64_t)(row0 + lr) * kWords;
       if (BITS == 4) {
@@ -829,12 +834,16 @@ __device__ __forceinline__ bool key_block(const unsigned char* tile, const Tenso
         for (uint32_t m = om; m; m &= m - 1) clear_field<PB>(wa, __ffs(m) - 1);
     }
     if (BITS == 3) {
-      // ten codes per word: the two rows of this step through the row buffer
-      unsigned char* rb = rowbuf + p * kHeadDim;
-      *reinterpret_cast<uint2*>(rb + 8 * o) = make_uint2(wa[0], wa[PB / 4 - 1]);
-      __syncwarp();
-      if (o < kWords) kdst[(int64_t)row * kWords + o] = pack3_word(rb, o);
-      __syncwarp();
+      // ten codes per word: the lane's 8 codes (channels 8 o ..) are 24 bits at
+      // bit 24 o of the row's stream; lane o writes word o
+      const uint32_t pw = comb4(wa[0]) | (comb4(wa[PB / 4 - 1]) << 12);
+      const int w = min(o, kWords - 1);
+      const int A = (5 * w) >> 2, oA = 30 * w - 24 * A;  // first source lane (0 .. 15), bit offset in it
+      const int hbase = lane & 16;
+      const uint32_t pa = __shfl_sync(kFull, pw, hbase + A);
+      const uint32_t pb = __shfl_sync(kFull, pw, hbase + min(A + 1, 15));
+      const uint32_t word = ((pa >> oA) | (A + 1 < 16 ? pb << (24 - oA) : 0u)) & 0x3FFFFFFFu;
+      if (o < kWords) kdst[(int64_t)row * kWords + o] = word;
     } else if (BITS == 4)
       kdst[(int64_t)row * kWords + o] = wa[0];
     else
@@ -877,7 +886,7 @@ struct Geo {
   static constexpr int kStages = 2;
   static constexpr int kMinBlocks = kStageBytes <= 16384 ? 5 : 3;
   static constexpr size_t kScratch = kPerChannel ? sizeof(KeyScratch<kW>) : 0;
-  static constexpr size_t kRowBuf = (KB == 3 || VB == 3) ? 4 * kHeadDim : 0;  // per warp, 3-bit repacking
+  static constexpr size_t kRowBuf = 0;  // per warp (the 3-bit codes are packed in registers)
   // per warp, the outlier masks of its key-block rows between the two passes
   static constexpr size_t kOmBuf = (kPerChannel && OUTL) ? (size_t)TB / kW / 2 * 32 * 2 : 0;
   static constexpr size_t kCtl = 64;  // counters and barriers
