@@ -88,6 +88,8 @@ _SIGNATURES = {
                         ctypes.POINTER(_P), _I, _P, ctypes.c_size_t, _P, _P],
     "kvq_cache_get_layout": [_P, _I, ctypes.POINTER(Layout)],
     "kvq_cache_length": [_P, _I, ctypes.POINTER(_I)],
+    "kvq_prefill_quantize_varlen": [_P, _I, _P, _P, _I, ctypes.POINTER(_I), _P],
+    "kvq_cache_seq_lengths": [_P, _I, ctypes.POINTER(_I)],
     "kvq_cache_status": [_P, _P, ctypes.POINTER(ctypes.c_uint32)],
     "kvq_selftest_div_levels": [_I, ctypes.c_uint32, ctypes.c_uint32, _P, _P],
     "kvq_selftest_code_rounding": [_I, _I, _I, _I, _P, _P],
@@ -233,6 +235,25 @@ class QuantizedKVCache:
         _check_half(v, (c.batch, c.num_kv_heads, s, c.head_dim), "v")
         check(lib().kvq_prefill_quantize(self.handle, layer, ctypes.c_void_p(k.data_ptr()),
                                          ctypes.c_void_p(v.data_ptr()), s, _stream_ptr(stream)))
+
+    def prefill_varlen(self, layer, k, v, lens, stream=None):
+        """Prefill from a padded batch in which batch row b holds lens[b] of
+        the k.shape[2] rows (kvq_prefill_quantize_varlen); later appends and
+        decodes of the layer use each row's own length."""
+        c = self.cfg
+        s = k.shape[2] if k.dim() == 4 else 0
+        _check_half(k, (c.batch, c.num_kv_heads, s, c.head_dim), "k")
+        _check_half(v, (c.batch, c.num_kv_heads, s, c.head_dim), "v")
+        if len(lens) != c.batch:
+            raise ValueError("one length per batch row")
+        arr = (ctypes.c_int32 * c.batch)(*[int(x) for x in lens])
+        check(lib().kvq_prefill_quantize_varlen(self.handle, layer, ctypes.c_void_p(k.data_ptr()),
+                                                ctypes.c_void_p(v.data_ptr()), s, arr, _stream_ptr(stream)))
+
+    def seq_lengths(self, layer):
+        arr = (ctypes.c_int32 * self.cfg.batch)()
+        check(lib().kvq_cache_seq_lengths(self.handle, layer, arr))
+        return list(arr)
 
     def append(self, layer, k1, v1, stream=None):
         c = self.cfg

@@ -169,7 +169,7 @@ cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t s
   if (decode_tc_supported(L, a.gqa)) {
     e = launch_decode_tc(L, a, st);
     combine = false;  // one split writes the output itself; the last CTA of a stream merges the splits
-  } else if (a.gqa == 1 && decode_mha_supported(L)) {
+  } else if (a.gqa == 1 && !a.varlen && decode_mha_supported(L)) {
     e = launch_decode_mha(L, a, st);
     combine = false;  // as above
   } else if (a.gqa > 1 && decode_gqa_supported(L, a.gqa)) {

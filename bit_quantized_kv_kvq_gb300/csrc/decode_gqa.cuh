@@ -153,9 +153,9 @@ __global__ void __launch_bounds__(kThreads, 3)
   float* ml = qf + 8 * kHeadDim;                     // [warps][8][2]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ml + kWarps * 16);
 
-  const int len = a.length, kq = a.k_quant_len;
+  const int len = a.varlen ? a.lens[b] : a.length, kq = a.k_quant_len;  // this batch row's tokens
   const int row_begin = split * a.tiles_per_split * kTile;
-  const int row_end = min(row_begin + a.tiles_per_split * kTile, len);
+  const int row_end = max(row_begin, min(row_begin + a.tiles_per_split * kTile, len));  // empty past a short row
   const int ntiles = (row_end - row_begin + kRows - 1) / kRows;
   const int per_warp = (ntiles + kWarps - 1) / kWarps;
   const int w_first = min(warp * per_warp, ntiles);

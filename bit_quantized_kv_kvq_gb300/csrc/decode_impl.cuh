@@ -93,11 +93,11 @@ __global__ void __launch_bounds__(kDecThreads)
   __shared__ float cbt[16];  // codebook levels (codebook codes only)
   if ((C::KCB || C::VCB) && tid < 16) cbt[tid] = __half2float(__ushort_as_half(L.codebook[tid]));
 
-  const int len = a.length, kq = a.k_quant_len;
+  const int len = a.varlen ? a.lens[b] : a.length, kq = a.k_quant_len;  // this batch row's tokens
   const int ntiles = (len + kTile - 1) / kTile;
   const int t_begin = split * a.tiles_per_split;
   const int t_end = min(t_begin + a.tiles_per_split, ntiles);
-  const int nt = t_end - t_begin;
+  const int nt = max(t_end - t_begin, 0);  // empty past a short batch row
   const int Gk = L.k.group, Gv = L.v.group;
   const int vgpr = kHeadDim / Gv;
   const int kgpr = C::KCH ? 1 : kHeadDim / Gk;

@@ -235,6 +235,7 @@ struct kvq_cache {
   int sm_count = 0;
   int device = 0;  // device that holds the buffer; launches need it current
   std::vector<cudaEvent_t> step_events;  // kvq_decode_step: one per layer + 1, made on first use
+  std::vector<std::vector<int32_t>> seq;  // per layer: the batch rows' own lengths (empty: all `len`)
   float cb_thr[16] = {};                 // codebook search table (codebook codes only)
   uint8_t cb_code[16] = {};
 
@@ -434,6 +435,7 @@ kvq_status kvq_cache_create_per_layer(const kvq_config* cfg, const int32_t* laye
   h->base = static_cast<unsigned char*>(dev_buf);
   h->bytes = bytes;
   h->len.assign(cfg->num_layers, 0);
+  h->seq.assign(cfg->num_layers, std::vector<int32_t>());
   h->sm_count = sms > 0 ? sms : 1;
   h->device = attr.device;
   *out = h;
@@ -479,6 +481,33 @@ kvq_status kvq_prefill_quantize(kvq_cache* h, int32_t layer, const void* k, cons
   if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
   if (nq > 0) kvq::count_launches(1);
   h->len[layer] = seq_len;
+  h->seq[layer].clear();
+  return KVQ_OK;
+}
+
+kvq_status kvq_prefill_quantize_varlen(kvq_cache* h, int32_t layer, const void* k, const void* v,
+                                       int32_t seq_len, const int32_t* lens, void* stream) {
+  kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  const kvq_config& c = h->cfg;
+  if (c.k_mode == KVQ_ASYM_PER_CHANNEL)
+    return fail(KVQ_ERR_UNSUPPORTED, "variable lengths need per-token keys (per-channel key blocks are per layer)");
+  if (c.sink_tokens > 0) return fail(KVQ_ERR_UNSUPPORTED, "variable lengths are not combined with sink tokens");
+  if (c.batch > kvq::kMaxVarlenBatch)
+    return fail(KVQ_ERR_UNSUPPORTED, "variable lengths take at most %d batch rows", kvq::kMaxVarlenBatch);
+  if (!lens) return fail(KVQ_ERR_INVALID_ARG, "lens must not be NULL");
+  int mx = 0;
+  for (int b = 0; b < c.batch; ++b) {
+    if (lens[b] < 1 || lens[b] > seq_len)
+      return fail(KVQ_ERR_INVALID_ARG, "lens[%d] = %d must be in [1, seq_len = %d]", b, lens[b], seq_len);
+    mx = lens[b] > mx ? lens[b] : mx;
+  }
+  // rows are coded independently: the padded rows past a batch row's length
+  // are coded too and overwritten by that row's later appends
+  s = kvq_prefill_quantize(h, layer, k, v, seq_len, stream);
+  if (s != KVQ_OK) return s;
+  h->seq[layer].assign(lens, lens + c.batch);
+  h->len[layer] = mx;
   return KVQ_OK;
 }
 
@@ -496,13 +525,31 @@ kvq_status kvq_append_quantize(kvq_cache* h, int32_t layer, const void* k, const
     return fail(KVQ_ERR_CAPACITY, "layer %d is full (%d tokens)", layer, pos);
   kvq::LayerDev L = layer_dev(h, layer);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<int32_t>& sq = h->seq[layer];
+  if (!sq.empty()) {  // variable lengths: each batch row appends at its own length
+    kvq::VarPos vp;
+    std::memset(&vp, 0, sizeof vp);
+    vp.on = 1;
+    vp.hkv = h->cfg.num_kv_heads;
+    for (int b = 0; b < h->cfg.batch; ++b) vp.pos[b] = sq[b];
+    cudaError_t e = kvq::launch_append(L, static_cast<const __half*>(k), static_cast<const __half*>(v), pos, vp, st);
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    kvq::count_launches(1);
+    int mx = 0;
+    for (int32_t& x : sq) mx = ++x > mx ? x : mx;
+    h->len[layer] = mx;
+    return KVQ_OK;
+  }
   if (pos < h->cfg.sink_tokens) {  // a sink token: kept in fp16 as it is
     cudaError_t e = copy_sink_rows(L, L.sink_k, k, 1, pos, 1, st);
     if (e == cudaSuccess) e = copy_sink_rows(L, L.sink_v, v, 1, pos, 1, st);
     if (e != cudaSuccess) return cuda_fail(e, "sink copy");
   } else {
+    kvq::VarPos none;
+    none.on = 0;
+    none.hkv = 1;
     cudaError_t e = kvq::launch_append(L, static_cast<const __half*>(k), static_cast<const __half*>(v),
-                                       pos - h->cfg.sink_tokens, st);
+                                       pos - h->cfg.sink_tokens, none, st);
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
     kvq::count_launches(1);
   }
@@ -582,6 +629,10 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
   a.gqa = gqa;
   a.num_q_heads = num_q_heads;
   a.sink_part = sink_part;
+  if (!h->seq[layer].empty()) {  // variable lengths (per-token keys): each batch row its own tokens
+    a.varlen = 1;
+    for (int b = 0; b < h->cfg.batch; ++b) a.lens[b] = h->seq[layer][b];
+  }
   if (kvq::decode_pipe_supported(L, gqa)) {
     const kvq::PipePlan pp = kvq::plan_decode_pipe(L, len, gqa, h->sm_count, h->splits_override);
     if (ws_bytes < pp.ws_bytes)
@@ -765,6 +816,14 @@ kvq_status kvq_cache_length(const kvq_cache* h, int32_t layer, int32_t* len) {
   if (s != KVQ_OK) return s;
   if (!len) return fail(KVQ_ERR_INVALID_ARG, "len is NULL");
   *len = h->len[layer];
+  return KVQ_OK;
+}
+
+kvq_status kvq_cache_seq_lengths(const kvq_cache* h, int32_t layer, int32_t* lens) {
+  kvq_status s = check_layer(h, layer);
+  if (s != KVQ_OK) return s;
+  if (!lens) return fail(KVQ_ERR_INVALID_ARG, "lens is NULL");
+  for (int b = 0; b < h->cfg.batch; ++b) lens[b] = h->seq[layer].empty() ? h->len[layer] : h->seq[layer][b];
   return KVQ_OK;
 }
 

@@ -64,6 +64,17 @@ struct LayerDev {
 // max|level| / 65536 apart, which check_config enforces.
 void codebook_search_table(const uint16_t levels[16], float thr[16], uint8_t code[16]);
 
+// Variable per-sequence lengths (per-token key codecs): each batch row b has
+// its own number of cached tokens; kernels read it from a fixed array.
+constexpr int kMaxVarlenBatch = 64;
+
+// Per-batch-row positions of an append (on: the rows' own lengths).
+struct VarPos {
+  int on;
+  int hkv;  // streams of a batch row: n / hkv is the row
+  int32_t pos[kMaxVarlenBatch];
+};
+
 constexpr int kMaxSinkTokens = 64;
 
 // Prefill attention over the cache (the last `chunk` positions' queries).
@@ -88,12 +99,12 @@ cudaError_t launch_prefill(const LayerDev& L, const __half* k, const __half* v, 
 // Codebook tensors (KVQ_CODEBOOK_PER_TOKEN, keys and values): rows
 // [row0, row0 + rows) of every stream from k, v fp16 [n][in_rows][D] (input
 // row i is coded row row0 + i).
-cudaError_t launch_codebook_rows(const LayerDev& L, const __half* k, const __half* v, int rows, int in_rows,
+cudaError_t launch_codebook_rows(const LayerDev& L, const __half* k, const __half* v, int rows, int in_rows, const VarPos& vp,
                                  int row0, cudaStream_t stream);
 
 // Append of one token at position pos (= length before the call): k1, v1
 // fp16 [n][D].
-cudaError_t launch_append(const LayerDev& L, const __half* k1, const __half* v1, int pos,
+cudaError_t launch_append(const LayerDev& L, const __half* k1, const __half* v1, int pos, const VarPos& vp,
                           cudaStream_t stream);
 
 struct DecodeArgs {
@@ -111,6 +122,8 @@ struct DecodeArgs {
   float* part_o;        // [B*Hq][splits][D]
   float* part_ml;       // [B*Hq][splits][2]
   int* occupancy_out;   // non-null: report resident CTAs per SM of the kernel, launch nothing
+  int varlen;           // lengths per batch row in lens (per-token keys only), else `length` for all
+  int32_t lens[kMaxVarlenBatch];
 };
 
 cudaError_t launch_decode(const LayerDev& L, const DecodeArgs& a, cudaStream_t stream);

@@ -30,8 +30,12 @@ static bool fast_prefill_supported(const LayerDev& L) {
 cudaError_t launch_prefill(const LayerDev& L, const __half* k, const __half* v, int seq_len,
                            cudaStream_t st) {
   if (seq_len <= 0) return cudaSuccess;
-  if (L.k.mode == KVQ_CODEBOOK_PER_TOKEN)
-    return launch_codebook_rows(L, k, v, seq_len, L.in_rows > 0 ? L.in_rows : seq_len, 0, st);
+  if (L.k.mode == KVQ_CODEBOOK_PER_TOKEN) {
+    VarPos none;
+    none.on = 0;
+    none.hkv = 1;
+    return launch_codebook_rows(L, k, v, seq_len, L.in_rows > 0 ? L.in_rows : seq_len, none, 0, st);
+  }
   if (fast_prefill_supported(L)) {
     const bool o = L.outliers > 0;
     if (L.v.bits == 3)

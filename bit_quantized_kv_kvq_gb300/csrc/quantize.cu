@@ -330,10 +330,12 @@ __device__ void quant_kblock(const BlockSmem& sm, int T, int t0, int blk, const 
 template <int KB, int KMODE, int VB, bool VSYM>
 __global__ void __launch_bounds__(256)
     append_kernel(LayerDev L, const __half* __restrict__ k1, const __half* __restrict__ v1,
-                  int pos) {
+                  int pos_all, const VarPos vp) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ __align__(16) uint8_t scratch[2][kHeadDim];
   const int n = blockIdx.x;
+  // the stream's row: its batch row's own length with variable lengths (per-token keys)
+  const int pos = vp.on ? vp.pos[n / vp.hkv] : pos_all;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const __half* kn = k1 + (int64_t)n * kHeadDim;
@@ -376,45 +378,46 @@ cudaError_t ensure_smem(F* kernel, size_t bytes) {
 }
 
 template <int KB, int KMODE, int VB, bool VSYM>
-cudaError_t launch_append_t(const LayerDev& L, const __half* k1, const __half* v1, int pos,
+cudaError_t launch_append_t(const LayerDev& L, const __half* k1, const __half* v1, int pos, const VarPos& vp,
                             cudaStream_t st) {
   size_t sm = 0;
   if (KMODE == KVQ_ASYM_PER_CHANNEL && (pos % L.k.group) == L.k.group - 1)
     sm = block_smem_bytes(L.k.group);
   cudaError_t e = ensure_smem(append_kernel<KB, KMODE, VB, VSYM>, sm);
   if (e != cudaSuccess) return e;
-  append_kernel<KB, KMODE, VB, VSYM><<<L.n_streams, 256, sm, st>>>(L, k1, v1, pos);
+  append_kernel<KB, KMODE, VB, VSYM><<<L.n_streams, 256, sm, st>>>(L, k1, v1, pos, vp);
   return cudaGetLastError();
 }
 
 template <int KB, int KMODE>
-cudaError_t launch_append_v(const LayerDev& L, const __half* k1, const __half* v1, int pos,
+cudaError_t launch_append_v(const LayerDev& L, const __half* k1, const __half* v1, int pos, const VarPos& vp,
                             cudaStream_t st) {
-  if (L.v.mode == KVQ_SYM_PER_TOKEN) return launch_append_t<KB, KMODE, 8, true>(L, k1, v1, pos, st);
+  if (L.v.mode == KVQ_SYM_PER_TOKEN) return launch_append_t<KB, KMODE, 8, true>(L, k1, v1, pos, vp, st);
   switch (L.v.bits) {
-    case 3: return launch_append_t<KB, KMODE, 3, false>(L, k1, v1, pos, st);
-    case 4: return launch_append_t<KB, KMODE, 4, false>(L, k1, v1, pos, st);
-    default: return launch_append_t<KB, KMODE, 8, false>(L, k1, v1, pos, st);
+    case 3: return launch_append_t<KB, KMODE, 3, false>(L, k1, v1, pos, vp, st);
+    case 4: return launch_append_t<KB, KMODE, 4, false>(L, k1, v1, pos, vp, st);
+    default: return launch_append_t<KB, KMODE, 8, false>(L, k1, v1, pos, vp, st);
   }
 }
 
 }  // namespace
 
-cudaError_t launch_append(const LayerDev& L, const __half* k1, const __half* v1, int pos,
+cudaError_t launch_append(const LayerDev& L, const __half* k1, const __half* v1, int pos, const VarPos& vp,
                           cudaStream_t st) {
-  if (L.k.mode == KVQ_CODEBOOK_PER_TOKEN) return launch_codebook_rows(L, k1, v1, 1, 1, pos, st);
-  if (L.k.mode == KVQ_SYM_PER_TOKEN) return launch_append_v<8, KVQ_SYM_PER_TOKEN>(L, k1, v1, pos, st);
+  if (vp.on && L.k.mode == KVQ_ASYM_PER_CHANNEL) return cudaErrorNotSupported;  // key blocks are per layer
+  if (L.k.mode == KVQ_CODEBOOK_PER_TOKEN) return launch_codebook_rows(L, k1, v1, 1, 1, vp, pos, st);
+  if (L.k.mode == KVQ_SYM_PER_TOKEN) return launch_append_v<8, KVQ_SYM_PER_TOKEN>(L, k1, v1, pos, vp, st);
   if (L.k.mode == KVQ_ASYM_PER_TOKEN) {
     switch (L.k.bits) {
-      case 3: return launch_append_v<3, KVQ_ASYM_PER_TOKEN>(L, k1, v1, pos, st);
-      case 4: return launch_append_v<4, KVQ_ASYM_PER_TOKEN>(L, k1, v1, pos, st);
-      default: return launch_append_v<8, KVQ_ASYM_PER_TOKEN>(L, k1, v1, pos, st);
+      case 3: return launch_append_v<3, KVQ_ASYM_PER_TOKEN>(L, k1, v1, pos, vp, st);
+      case 4: return launch_append_v<4, KVQ_ASYM_PER_TOKEN>(L, k1, v1, pos, vp, st);
+      default: return launch_append_v<8, KVQ_ASYM_PER_TOKEN>(L, k1, v1, pos, vp, st);
     }
   }
   switch (L.k.bits) {
-    case 3: return launch_append_v<3, KVQ_ASYM_PER_CHANNEL>(L, k1, v1, pos, st);
-    case 4: return launch_append_v<4, KVQ_ASYM_PER_CHANNEL>(L, k1, v1, pos, st);
-    default: return launch_append_v<8, KVQ_ASYM_PER_CHANNEL>(L, k1, v1, pos, st);
+    case 3: return launch_append_v<3, KVQ_ASYM_PER_CHANNEL>(L, k1, v1, pos, vp, st);
+    case 4: return launch_append_v<4, KVQ_ASYM_PER_CHANNEL>(L, k1, v1, pos, vp, st);
+    default: return launch_append_v<8, KVQ_ASYM_PER_CHANNEL>(L, k1, v1, pos, vp, st);
   }
 }
 

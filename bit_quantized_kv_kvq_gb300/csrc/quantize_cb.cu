@@ -73,7 +73,7 @@ __device__ __forceinline__ void code_row(const TensorDev& T, int n, int r, uint2
 // two rows in flight per warp.
 __global__ void __launch_bounds__(32 * kRowsPerCta)
     codebook_rows_kernel(LayerDev L, const __half* __restrict__ k, const __half* __restrict__ v, int rows,
-                         int in_rows, int row0) {
+                         int in_rows, const VarPos vp, int row0_all) {
   __shared__ float thr[16];
   __shared__ uint32_t code[16];
   if (threadIdx.x < 16) {
@@ -84,6 +84,7 @@ __global__ void __launch_bounds__(32 * kRowsPerCta)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int n = blockIdx.y;
   const bool is_k = blockIdx.z == 0;
+  const int row0 = vp.on ? vp.pos[n / vp.hkv] : row0_all;  // per batch row with variable lengths
   const TensorDev& T = is_k ? L.k : L.v;
   const __half* src = (is_k ? k : v) + (int64_t)n * in_rows * kHeadDim + 4 * lane;
   float cbmax = 0.0f;
@@ -158,14 +159,14 @@ void codebook_search_table(const uint16_t levels[16], float thr[16], uint8_t cod
 }
 
 cudaError_t launch_codebook_rows(const LayerDev& L, const __half* k, const __half* v, int rows, int in_rows,
-                                 int row0, cudaStream_t stream) {
+                                 const VarPos& vp, int row0, cudaStream_t stream) {
   if (rows <= 0) return cudaSuccess;
   // about 1216 CTAs of 8 warps in all (eight per SM), more when few streams
   int gx = (rows + kRowsPerCta - 1) / kRowsPerCta;
   const int cap = 1216 / (2 * L.n_streams) > 1 ? 1216 / (2 * L.n_streams) : 1;
   if (gx > cap) gx = cap;
   const dim3 grid(gx, L.n_streams, 2);
-  codebook_rows_kernel<<<grid, 32 * kRowsPerCta, 0, stream>>>(L, k, v, rows, in_rows, row0);
+  codebook_rows_kernel<<<grid, 32 * kRowsPerCta, 0, stream>>>(L, k, v, rows, in_rows, vp, row0);
   return cudaGetLastError();
 }
 

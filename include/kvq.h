@@ -305,6 +305,28 @@ KVQ_API kvq_status kvq_prefill_attention(kvq_cache* cache, int32_t layer, const 
                                          int32_t num_q_heads, float softmax_scale, void* out,
                                          int32_t out_dtype, void* stream);
 
+/* Variable per-sequence lengths in a batch. Prefills layer `layer` from a
+ * padded batch (k, v as in kvq_prefill_quantize, seq_len rows per stream)
+ * in which batch row b holds lens[b] tokens (host array of cfg.batch
+ * entries, 1 <= lens[b] <= seq_len); the rows past lens[b] are ignored.
+ * From then on every kvq_append_quantize of the layer appends each batch
+ * row's new token at that row's own length, and kvq_decode_attention
+ * attends each batch row's own tokens, until the next kvq_prefill_quantize
+ * of the layer makes the lengths equal again. kvq_cache_length reports the
+ * largest length; kvq_cache_seq_lengths the rows' own.
+ * Per-token key codecs only (symmetric, asymmetric per token, codebook):
+ * every row is coded on its own, while per-channel key blocks span a whole
+ * layer (KVQ_ERR_UNSUPPORTED for per-channel keys, for caches with sink
+ * tokens and for more than 64 batch rows).
+ * Errors: KVQ_ERR_INVALID_ARG for a NULL lens or a length out of range. */
+KVQ_API kvq_status kvq_prefill_quantize_varlen(kvq_cache* cache, int32_t layer, const void* k, const void* v,
+                                               int32_t seq_len, const int32_t* lens, void* stream);
+
+/* The tokens of each batch row of layer `layer` (host array of cfg.batch
+ * entries): the rows' own lengths after kvq_prefill_quantize_varlen, else
+ * the layer's length for every row (host mirror, no sync). */
+KVQ_API kvq_status kvq_cache_seq_lengths(const kvq_cache* cache, int32_t layer, int32_t* lens);
+
 /* Forces the number of sequence splits of later decode calls (0 = automatic):
  * for the stream-K decode the number of persistent CTAs (at most one per SM),
  * otherwise the splits per stream. Results agree for every count up to
