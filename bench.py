@@ -268,7 +268,10 @@ class Model:
         kv0 = None
         for l in range(self.wl.num_layers):
             k, v = self.src[l].kv(self.S)
-            self.cache.prefill(l, k, v)
+            if self.wl.lens:  # a ragged batch: each row keeps its own tokens
+                self.cache.prefill_varlen(l, k, v, list(self.wl.lens))
+            else:
+                self.cache.prefill(l, k, v)
             if l == 0:
                 kv0 = (k, v)
             else:
@@ -394,7 +397,10 @@ def run_gpu(args, wl, rank, world, device):
         a0 = torch.cuda.Event(enable_timing=True)
         a1 = torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        cache.prefill(0, k0, v0)
+        if wl.lens:
+            cache.prefill_varlen(0, k0, v0, list(wl.lens))
+        else:
+            cache.prefill(0, k0, v0)
         a1.record(stream)
         torch.cuda.synchronize(device)
         if i >= 3:
@@ -405,7 +411,7 @@ def run_gpu(args, wl, rank, world, device):
     del k0, v0
     torch.cuda.synchronize(device)
 
-    pattn = prefill_attention_timing(wl, model, device, flush)
+    pattn = None if wl.lens else prefill_attention_timing(wl, model, device, flush)
     e2e = run_e2e(args, wl, model, st, device)
     err = e2e_error(wl, model, device)
 
@@ -420,6 +426,7 @@ def run_gpu(args, wl, rank, world, device):
                    "k_codec": codec_name(wl.k_bits, wl.k_mode, wl.k_group),
                    "v_codec": codec_name(wl.v_bits, wl.v_mode, wl.v_group),
                    "outliers_per_row": wl.outliers_per_row,
+                   "row_lengths": list(wl.lens) if wl.lens else None,
                    "step": "append_quantize on every layer, then decode_attention on every layer",
                    "l2": ("flushed before each step (256 MB written then read); one layer's cache is %.0f MB"
                           % (per_layer / 1e6)) if need_flush else

@@ -10,6 +10,8 @@ Split-K partials are workspace traffic, not algorithmic bytes.
 """
 from __future__ import annotations
 
+from dataclasses import replace
+
 from .workloads import ASYM_PER_CHANNEL, CODEBOOK_PER_TOKEN, SYM_PER_TOKEN
 
 
@@ -46,9 +48,22 @@ def cache_read_bytes(wl, length):
     return total
 
 
+def row_lengths(wl, length):
+    """Tokens of each batch row when the longest holds `length` (a ragged
+    batch's rows all grow by one token per append)."""
+    if not wl.lens:
+        return [length] * wl.batch
+    return [x + length - max(wl.lens) for x in wl.lens]
+
+
 def decode_bytes(wl, length):
-    return (cache_read_bytes(wl, length) + wl.batch * wl.num_q_heads * wl.head_dim * 2
-            + wl.batch * wl.num_q_heads * wl.head_dim * 4)
+    """One decode over every batch row's own tokens (the longest: `length`)."""
+    if wl.lens:
+        one = replace(wl, batch=1, lens=None)
+        cache = sum(cache_read_bytes(one, n) for n in row_lengths(wl, length))
+    else:
+        cache = cache_read_bytes(wl, length)
+    return cache + wl.batch * wl.num_q_heads * wl.head_dim * 2 + wl.batch * wl.num_q_heads * wl.head_dim * 4
 
 
 def prefill_bytes(wl, length):

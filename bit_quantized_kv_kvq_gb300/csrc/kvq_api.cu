@@ -328,7 +328,11 @@ int k_quant_len(const kvq_config& c, int len) {
 // the merge of a stream's partials by its last CTA (one round of loads per
 // 16 partials); the split count minimizing it balances wave quantization
 // against short CTAs and long merges.
-void plan_splits(const kvq_cache* h, int len, int slots, int* splits, int* tiles_per_split) {
+// lens: the batch rows' own lengths (variable lengths), or NULL when every
+// row holds `len` tokens. With variable lengths a row of n tiles keeps
+// ceil(n / tps) CTAs busy; the others of its grid row find no tiles.
+void plan_splits(const kvq_cache* h, int len, int slots, int* splits, int* tiles_per_split,
+                 const int32_t* lens = nullptr) {
   const int ntiles = (len + kvq::kTile - 1) / kvq::kTile;
   if (h->splits_override > 0) {
     int want = h->splits_override < ntiles ? h->splits_override : ntiles;
@@ -347,10 +351,17 @@ void plan_splits(const kvq_cache* h, int len, int slots, int* splits, int* tiles
     const int tps = (ntiles + s - 1) / s;
     const int s2 = (ntiles + tps - 1) / tps;
     if (s2 != s) continue;  // same shape as a smaller s
-    const int64_t ctas = n * s2;
+    int64_t ctas = n * s2;
+    double empty_rows = 0.0;  // CTAs past a short row still load the query and write an empty partial
+    if (lens) {  // only the CTAs that hold tiles of their row do the work
+      ctas = 0;
+      for (int b = 0; b < h->cfg.batch; ++b)
+        ctas += (int64_t)h->cfg.num_kv_heads * (((lens[b] + kvq::kTile - 1) / kvq::kTile + tps - 1) / tps);
+      empty_rows = 96.0 * (double)(n * s2 - ctas) / (double)slots;
+    }
     const int64_t waves = (ctas + slots - 1) / slots;
     const double merge_rows = s2 > 1 ? 48.0 * (double)((s2 + 15) / 16) : 0.0;
-    const double t = (double)waves * ((double)tps * kvq::kTile + fixed_rows) + merge_rows;
+    const double t = (double)waves * ((double)tps * kvq::kTile + fixed_rows) + merge_rows + empty_rows;
     if (t < best * 0.999) {
       best = t;
       best_s = s2;
@@ -654,7 +665,7 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
   if (e != cudaSuccess) return cuda_fail(e, "decode occupancy query");
   a.occupancy_out = nullptr;
   int splits = 1, tps = 1;
-  plan_splits(h, len, h->sm_count * (occ > 0 ? occ : 1), &splits, &tps);
+  plan_splits(h, len, h->sm_count * (occ > 0 ? occ : 1), &splits, &tps, a.varlen ? a.lens : nullptr);
   const size_t need = workspace_for(h, num_q_heads, splits);
   if (ws_bytes < need)
     return fail(KVQ_ERR_BUFFER_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, need);
@@ -693,6 +704,8 @@ kvq_status kvq_prefill_attention(kvq_cache* h, int32_t layer, const void* q, int
   if (len == 0) return fail(KVQ_ERR_INVALID_ARG, "layer %d is empty: attention is undefined", layer);
   if (chunk < 1 || chunk > len)
     return fail(KVQ_ERR_INVALID_ARG, "chunk %d must be in [1, %d] (the tokens cached)", chunk, len);
+  if (!h->seq[layer].empty())
+    return fail(KVQ_ERR_UNSUPPORTED, "prefill attention over a layer with variable lengths is not built");
   if ((int64_t)chunk * (num_q_heads / hkv) > ((int64_t)1 << 30))
     return fail(KVQ_ERR_INVALID_ARG, "chunk * query heads per kv-head is too large");
   kvq::PrefillAttnArgs a;

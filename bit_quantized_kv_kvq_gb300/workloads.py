@@ -1,5 +1,5 @@
 """The five seeded synthetic workloads, described by shape and codec, and
-the codebook-codec layer beside them.
+the codebook-codec layer and the ragged batch beside them.
 
 Each entry names what it is: the tiny q8_0-style GQA layer, the
 Llama-2-7B-shaped MHA layer (two contexts), the Llama-2-70B-shaped GQA layer
@@ -37,6 +37,7 @@ class Workload:
     decode_steps: int = 1
     dist: str = "normal"  # normal | k_lognormal_channels | k_heavy15 | t3_heavy20
     codebook: tuple = None  # 16 levels of CODEBOOK_PER_TOKEN tensors
+    lens: tuple = None      # ragged batch: each row's tokens at the prefill (seq_len = the longest)
 
     @property
     def gqa(self):
@@ -81,6 +82,12 @@ LLAMA8B_E2M1 = Workload("8b-layer-h32x8-s131072-e2m1-g32", 5, 1, 1, 32, 8, 128, 
                         4, 4, CODEBOOK_PER_TOKEN, CODEBOOK_PER_TOKEN, 32, 32, decode_steps=64,
                         dist="k_lognormal_channels", codebook=E2M1)
 
+# A ragged batch of eight q8_0-style sequences (int8 per-token keys and
+# values, 8 kv-heads, 4 query heads per kv-head) from 512 to 32768 tokens.
+RAGGED_Q8 = Workload("q8_0-gqa4-b8x8-ragged-s32768", 6, 1, 8, 32, 8, 128, 32768,
+                     8, 8, SYM_PER_TOKEN, SYM_PER_TOKEN, 32, 32, decode_steps=64, dist="normal",
+                     lens=(32768, 4096, 16384, 1024, 28672, 8192, 512, 20480))
+
 ALL = [TINY_Q8, LLAMA7B_8K, LLAMA7B_16K, LLAMA70B_32K, DENSE_SPARSE_128K, LLAMA8B_FULL]
-EXTRA = [LLAMA8B_E2M1]
+EXTRA = [LLAMA8B_E2M1, RAGGED_Q8]
 BY_NAME = {w.name: w for w in ALL + EXTRA}

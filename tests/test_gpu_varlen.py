@@ -103,6 +103,8 @@ def test_uniform_prefill_ends_variable_lengths():
     k, v = LayerSource(wl, 0, device="cpu").kv(64)
     cache = K.make_gpu_cache(wl, 80)
     cache.prefill_varlen(0, k.cuda(), v.cuda(), [3, 64, 9, 10])
+    with pytest.raises(kvq.KVQError):  # prefill attention over ragged rows is not built
+        cache.prefill_attention(0, torch.zeros((4, 2, 8, 128), dtype=torch.float16, device="cuda"), 1.0)
     cache.prefill(0, k.cuda(), v.cuda())
     assert cache.seq_lengths(0) == [64, 64, 64, 64]
 

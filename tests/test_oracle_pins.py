@@ -784,3 +784,16 @@ def test_prefill_attention_last_query_is_the_decode():
     np.testing.assert_array_equal(oc.prefill_attention(q[:, -1:], 0.1)[:, 0], oc.decode(q[:, -1], 0.1))
     with pytest.raises(ValueError):
         oc.prefill_attention(rng.standard_normal((2, 151, 4, 128)), 0.1)
+
+
+def test_ragged_decode_bytes_are_the_rows_own():
+    """A ragged batch's decode bytes are the footprint of each row's own
+    tokens (one-row caches of those lengths) plus the queries and outputs."""
+    from bit_quantized_kv_kvq_gb300 import accounting as A, workloads as W
+    wl = W.RAGGED_Q8
+    for extra in (0, 1, 64):
+        L = max(wl.lens) + extra
+        want = sum(O.packed_cache_bytes(1, 1, wl.num_kv_heads, wl.head_dim, n + extra, wl.k_bits, wl.v_bits,
+                                        wl.k_mode, wl.v_mode, wl.k_group, wl.v_group) for n in wl.lens)
+        want += wl.batch * wl.num_q_heads * wl.head_dim * 6
+        assert A.decode_bytes(wl, L) == want
