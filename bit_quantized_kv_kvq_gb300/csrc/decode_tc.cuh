@@ -145,9 +145,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
   float* ml = qm + HQ * kHeadDim;                                 // [warps][H][2]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ml + kWarps * H * 2);
 
-  const int len = a.length, kq = a.k_quant_len;
+  // variable lengths: this batch row's tokens and its quantized key blocks
+  const int len = a.varlen ? a.lens[b] : a.length;
+  const int kq = a.varlen ? len / L.k.group * L.k.group : a.k_quant_len;
   const int row_begin = split * a.tiles_per_split * kTile;
-  const int row_end = min(row_begin + a.tiles_per_split * kTile, len);
+  const int row_end = max(row_begin, min(row_begin + a.tiles_per_split * kTile, len));  // empty past a short row
   const int ntiles = (row_end - row_begin + kRows - 1) / kRows;
   const int per_warp = (ntiles + kWarps - 1) / kWarps;
   const int w_first = min(warp * per_warp, ntiles);

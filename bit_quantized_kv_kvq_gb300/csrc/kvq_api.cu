@@ -304,6 +304,23 @@ kvq::LayerDev layer_dev(const kvq_cache* h, int layer) {
   return L;
 }
 
+// The streams of batch row b alone (its num_kv_heads streams) as a layer:
+// every per-stream array starts at the row's first stream.
+kvq::LayerDev row_view(const kvq::LayerDev& L, int b) {
+  kvq::LayerDev R = L;
+  const int64_t s0 = (int64_t)b * L.num_kv_heads;
+  for (kvq::TensorDev* T : {&R.k, &R.v}) {
+    T->codes += s0 * T->codes_sstride;
+    T->meta += s0 * T->meta_sstride;
+    if (T->resid) T->resid += s0 * T->resid_sstride;
+    if (T->rowptr) T->rowptr += s0 * T->rowptr_sstride;
+    if (T->col) T->col += s0 * T->out_sstride;
+    if (T->val) T->val += s0 * T->out_sstride;
+  }
+  R.n_streams = L.num_kv_heads;
+  return R;
+}
+
 // Tokens of a layer held as sinks, and the tokens after them (the coded rows).
 int sink_len(const kvq_config& c, int len) { return len < c.sink_tokens ? len : c.sink_tokens; }
 int coded_len(const kvq_config& c, int len) { return len - sink_len(c, len); }
@@ -501,8 +518,6 @@ kvq_status kvq_prefill_quantize_varlen(kvq_cache* h, int32_t layer, const void* 
   kvq_status s = check_layer(h, layer);
   if (s != KVQ_OK) return s;
   const kvq_config& c = h->cfg;
-  if (c.k_mode == KVQ_ASYM_PER_CHANNEL)
-    return fail(KVQ_ERR_UNSUPPORTED, "variable lengths need per-token keys (per-channel key blocks are per layer)");
   if (c.sink_tokens > 0) return fail(KVQ_ERR_UNSUPPORTED, "variable lengths are not combined with sink tokens");
   if (c.batch > kvq::kMaxVarlenBatch)
     return fail(KVQ_ERR_UNSUPPORTED, "variable lengths take at most %d batch rows", kvq::kMaxVarlenBatch);
@@ -513,10 +528,31 @@ kvq_status kvq_prefill_quantize_varlen(kvq_cache* h, int32_t layer, const void* 
       return fail(KVQ_ERR_INVALID_ARG, "lens[%d] = %d must be in [1, seq_len = %d]", b, lens[b], seq_len);
     mx = lens[b] > mx ? lens[b] : mx;
   }
-  // rows are coded independently: the padded rows past a batch row's length
-  // are coded too and overwritten by that row's later appends
-  s = kvq_prefill_quantize(h, layer, k, v, seq_len, stream);
-  if (s != KVQ_OK) return s;
+  if (c.k_mode == KVQ_ASYM_PER_CHANNEL) {
+    // per-channel key blocks start at each row's first token: one prefill per
+    // batch row over its own tokens (its key blocks and fp16 residual)
+    s = check_device(h);
+    if (s != KVQ_OK) return s;
+    if (seq_len > c.max_seq) return fail(KVQ_ERR_CAPACITY, "seq_len %d exceeds max_seq %d", seq_len, c.max_seq);
+    if (!k || !v) return fail(KVQ_ERR_INVALID_ARG, "k and v must not be NULL");
+    if (!aligned(k, 16) || !aligned(v, 16)) return fail(KVQ_ERR_INVALID_ARG, "k and v must be 16-byte aligned");
+    const kvq::LayerDev L = layer_dev(h, layer);
+    const size_t row_elems = (size_t)c.num_kv_heads * seq_len * kvq::kHeadDim;
+    for (int b = 0; b < c.batch; ++b) {
+      kvq::LayerDev Lb = row_view(L, b);
+      Lb.in_rows = seq_len;
+      const cudaError_t e = kvq::launch_prefill(Lb, static_cast<const __half*>(k) + b * row_elems,
+                                                static_cast<const __half*>(v) + b * row_elems, lens[b],
+                                                static_cast<cudaStream_t>(stream));
+      if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+      kvq::count_launches(1);
+    }
+  } else {
+    // rows are coded independently: the padded rows past a batch row's length
+    // are coded too and overwritten by that row's later appends
+    s = kvq_prefill_quantize(h, layer, k, v, seq_len, stream);
+    if (s != KVQ_OK) return s;
+  }
   h->seq[layer].assign(lens, lens + c.batch);
   h->len[layer] = mx;
   return KVQ_OK;
@@ -542,6 +578,7 @@ kvq_status kvq_append_quantize(kvq_cache* h, int32_t layer, const void* k, const
     std::memset(&vp, 0, sizeof vp);
     vp.on = 1;
     vp.hkv = h->cfg.num_kv_heads;
+    vp.rows = h->cfg.batch;
     for (int b = 0; b < h->cfg.batch; ++b) vp.pos[b] = sq[b];
     cudaError_t e = kvq::launch_append(L, static_cast<const __half*>(k), static_cast<const __half*>(v), pos, vp, st);
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
@@ -580,9 +617,8 @@ kvq_status kvq_decode_workspace_bytes(const kvq_cache* h, int32_t num_q_heads, s
     if (num_q_heads % hkv == 0 && kvq::decode_pipe_supported(L, num_q_heads / hkv)) {
       const size_t b = kvq::decode_pipe_workspace_max(L, num_q_heads / hkv, h->sm_count);
       if (b > need) need = b;
-    } else {
-      split = true;
     }
+    split = true;  // the split decode serves every layer with variable lengths
   }
   if (split) {
     const int max_splits = h->plan.capacity / kvq::kTile;  // one tile per split at most
@@ -640,11 +676,11 @@ kvq_status kvq_decode_attention(kvq_cache* h, int32_t layer, const void* q, int3
   a.gqa = gqa;
   a.num_q_heads = num_q_heads;
   a.sink_part = sink_part;
-  if (!h->seq[layer].empty()) {  // variable lengths (per-token keys): each batch row its own tokens
+  if (!h->seq[layer].empty()) {  // variable lengths: each batch row its own tokens
     a.varlen = 1;
     for (int b = 0; b < h->cfg.batch; ++b) a.lens[b] = h->seq[layer][b];
   }
-  if (kvq::decode_pipe_supported(L, gqa)) {
+  if (kvq::decode_pipe_supported(L, gqa) && !a.varlen) {  // stream-K cuts equal-length streams
     const kvq::PipePlan pp = kvq::plan_decode_pipe(L, len, gqa, h->sm_count, h->splits_override);
     if (ws_bytes < pp.ws_bytes)
       return fail(KVQ_ERR_BUFFER_TOO_SMALL, "workspace has %zu bytes, needs %zu", ws_bytes, pp.ws_bytes);

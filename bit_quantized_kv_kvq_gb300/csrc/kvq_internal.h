@@ -71,7 +71,8 @@ constexpr int kMaxVarlenBatch = 64;
 // Per-batch-row positions of an append (on: the rows' own lengths).
 struct VarPos {
   int on;
-  int hkv;  // streams of a batch row: n / hkv is the row
+  int hkv;   // streams of a batch row: n / hkv is the row
+  int rows;  // batch rows
   int32_t pos[kMaxVarlenBatch];
 };
 

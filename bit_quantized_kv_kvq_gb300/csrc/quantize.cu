@@ -381,8 +381,14 @@ template <int KB, int KMODE, int VB, bool VSYM>
 cudaError_t launch_append_t(const LayerDev& L, const __half* k1, const __half* v1, int pos, const VarPos& vp,
                             cudaStream_t st) {
   size_t sm = 0;
-  if (KMODE == KVQ_ASYM_PER_CHANNEL && (pos % L.k.group) == L.k.group - 1)
-    sm = block_smem_bytes(L.k.group);
+  if (KMODE == KVQ_ASYM_PER_CHANNEL) {  // a key block fills (in some row, with variable lengths)
+    bool flush = (pos % L.k.group) == L.k.group - 1;
+    if (vp.on) {
+      flush = false;
+      for (int b = 0; b < vp.rows; ++b) flush = flush || (vp.pos[b] % L.k.group) == L.k.group - 1;
+    }
+    if (flush) sm = block_smem_bytes(L.k.group);
+  }
   cudaError_t e = ensure_smem(append_kernel<KB, KMODE, VB, VSYM>, sm);
   if (e != cudaSuccess) return e;
   append_kernel<KB, KMODE, VB, VSYM><<<L.n_streams, 256, sm, st>>>(L, k1, v1, pos, vp);
@@ -404,7 +410,6 @@ cudaError_t launch_append_v(const LayerDev& L, const __half* k1, const __half* v
 
 cudaError_t launch_append(const LayerDev& L, const __half* k1, const __half* v1, int pos, const VarPos& vp,
                           cudaStream_t st) {
-  if (vp.on && L.k.mode == KVQ_ASYM_PER_CHANNEL) return cudaErrorNotSupported;  // key blocks are per layer
   if (L.k.mode == KVQ_CODEBOOK_PER_TOKEN) return launch_codebook_rows(L, k1, v1, 1, 1, vp, pos, st);
   if (L.k.mode == KVQ_SYM_PER_TOKEN) return launch_append_v<8, KVQ_SYM_PER_TOKEN>(L, k1, v1, pos, vp, st);
   if (L.k.mode == KVQ_ASYM_PER_TOKEN) {

@@ -315,10 +315,12 @@ KVQ_API kvq_status kvq_prefill_attention(kvq_cache* cache, int32_t layer, const 
  * attends each batch row's own tokens, until the next kvq_prefill_quantize
  * of the layer makes the lengths equal again. kvq_cache_length reports the
  * largest length; kvq_cache_seq_lengths the rows' own.
- * Per-token key codecs only (symmetric, asymmetric per token, codebook):
- * every row is coded on its own, while per-channel key blocks span a whole
- * layer (KVQ_ERR_UNSUPPORTED for per-channel keys, for caches with sink
- * tokens and for more than 64 batch rows).
+ * Every codec: per-token rows are coded on their own; per-channel key
+ * blocks start at each row's first token (one prefill launch per batch row
+ * then), so a row's fp16 key residual fills and flushes at its own appends.
+ * Decodes of such a layer take the split-K kernels (not the stream-K one).
+ * KVQ_ERR_UNSUPPORTED for caches with sink tokens and for more than 64
+ * batch rows.
  * Errors: KVQ_ERR_INVALID_ARG for a NULL lens or a length out of range. */
 KVQ_API kvq_status kvq_prefill_quantize_varlen(kvq_cache* cache, int32_t layer, const void* k, const void* v,
                                                int32_t seq_len, const int32_t* lens, void* stream);

@@ -4,8 +4,9 @@ each row's own length, and decodes over each row's own tokens. The CUDA path
 against one oracle cache per stream built from that stream's tokens alone:
 codes, scales and outliers of each stream's rows bit-exact, attention within
 1e-3, through the GQA tensor-core kernel and the generic kernel, the
-two-stream decode step, and the refusals (per-channel keys, sinks, lengths
-out of range)."""
+two-stream decode step, per-channel keys whose residual fills and flushes
+a block at each row's own appends, and the refusals (sinks, lengths out of
+range, prefill attention over ragged rows)."""
 import math
 from dataclasses import replace
 
@@ -32,21 +33,51 @@ CASES = [
     ("asym k3v3 g4", W.LLAMA70B_32K, 4, dict(k_mode=PT)),
 ]
 LENS = [37, 200, 1, 130]
+# per-channel keys: rows whose key residual fills (and flushes a block) during the appends
+PC_CASES = [
+    ("per-channel k4v8 T64 g4", W.LLAMA8B_FULL, 4, [62, 200, 1, 127]),
+    ("per-channel k3v3 T128 g8", W.LLAMA70B_32K, 8, [126, 200, 1, 130]),
+    ("per-channel k4v4 outliers g1", W.DENSE_SPARSE_128K, 1, [62, 150, 3, 64]),
+]
 
 
-def state_rows(cache, n, rows, kout):
-    """The per-token arrays of stream n's first `rows` rows."""
+def state_rows(cache, wl, n, rows):
+    """The arrays of stream n holding its first `rows` tokens (per-channel
+    keys: its own key blocks and fp16 residual)."""
+    lo = cache.layout(0)
+    D = wl.head_dim
     st = K.gpu_state(cache, 0, n)
-    out = {key: st[key][:rows] for key in ("k_words", "v_words", "k_meta", "v_meta")}
+    out = {key: st[key][:rows] for key in ("v_words", "v_meta")}
+    kout = wl.outliers_per_row
+    if wl.k_mode == W.ASYM_PER_CHANNEL:
+        kq = rows // wl.k_group * wl.k_group
+        wk = lo.k_words_per_row
+        out["k_words"] = K._bytes(cache, lo.k_codes + n * lo.k_codes_stream_bytes, kq * wk * 4).view(
+            np.uint32).reshape(kq, wk)
+        nb = kq // wl.k_group
+        out["k_meta"] = K._bytes(cache, lo.k_meta + n * lo.k_meta_stream_bytes, nb * D * 4).view(
+            np.uint16).reshape(nb, D, 2)
+        r = rows - kq
+        out["k_resid"] = K._bytes(cache, lo.k_resid + n * lo.k_resid_stream_bytes, r * D * 2).view(
+            np.float16).reshape(r, D)
+        krows = kq
+    else:
+        out["k_words"] = st["k_words"][:rows]
+        out["k_meta"] = st["k_meta"][:rows]
+        krows = rows
     if kout:
-        for t in ("k", "v"):
-            out[t + "_rowptr"] = st[t + "_rowptr"][:rows + 1]
-            out[t + "_col"] = st[t + "_col"][:rows * kout]
-            out[t + "_val"] = st[t + "_val"][:rows * kout]
+        for t, nr in (("k", krows), ("v", rows)):
+            rp = getattr(lo, t + "_out_rowptr")
+            col = getattr(lo, t + "_out_col")
+            val = getattr(lo, t + "_out_val")
+            out[t + "_rowptr"] = K._bytes(cache, rp + n * lo.out_rowptr_stream_bytes, (nr + 1) * 4).view(np.int32)
+            out[t + "_col"] = K._bytes(cache, col + n * lo.out_col_stream_bytes, nr * kout * 2).view(np.uint16)
+            out[t + "_val"] = K._bytes(cache, val + n * lo.out_val_stream_bytes, nr * kout * 2).view(np.float16)
     return out
 
 
-def run_case(wl0, g, over, steps=3, use_step=False):
+def run_case(wl0, g, over, steps=3, use_step=False, lens=LENS):
+    LENS = lens
     wl = replace(wl0, num_layers=1, batch=len(LENS), num_kv_heads=2, num_q_heads=2 * g,
                  seq_len=max(LENS), **over)
     S, H = wl.seq_len, wl.num_kv_heads
@@ -83,8 +114,7 @@ def run_case(wl0, g, over, steps=3, use_step=False):
     assert cache.seq_lengths(0) == [x + steps for x in LENS]
     for n, oc in enumerate(ocs):
         b = n // H
-        K.assert_state_equal(state_rows(cache, n, LENS[b] + steps, wl.outliers_per_row), K.oracle_state(oc, 0),
-                             "stream %d" % n)
+        K.assert_state_equal(state_rows(cache, wl, n, LENS[b] + steps), K.oracle_state(oc, 0), "stream %d" % n)
     assert cache.status() == 0
 
 
@@ -92,6 +122,12 @@ def run_case(wl0, g, over, steps=3, use_step=False):
 def test_varlen_against_per_stream_oracles(case):
     name, wl0, g, over = case
     run_case(wl0, g, over)
+
+
+@pytest.mark.parametrize("case", PC_CASES, ids=lambda c: c[0])
+def test_varlen_per_channel_keys(case):
+    name, wl0, g, lens = case
+    run_case(wl0, g, {}, lens=lens)
 
 
 def test_varlen_through_the_two_stream_step():
@@ -112,9 +148,6 @@ def test_uniform_prefill_ends_variable_lengths():
 def test_varlen_refusals():
     wl = replace(W.LLAMA8B_FULL, num_layers=1, batch=2, num_kv_heads=2, num_q_heads=4, seq_len=16)
     k, v = LayerSource(wl, 0, device="cpu").kv(16)
-    per_channel = K.make_gpu_cache(wl, 32)
-    with pytest.raises(kvq.KVQError):
-        per_channel.prefill_varlen(0, k.cuda(), v.cuda(), [4, 16])       # per-channel key blocks
     tok = replace(W.TINY_Q8, num_layers=1, batch=2, num_kv_heads=2, num_q_heads=4, seq_len=16)
     cache = K.make_gpu_cache(tok, 32)
     with pytest.raises(kvq.KVQError):
