@@ -124,7 +124,8 @@ def prefill_attention_timing(wl, model, device, flush, chunk=1024, reps=3):
     each)."""
     cache = model.cache
     S = model.length()
-    chunk = min(chunk, S)
+    rows = cache.seq_lengths(0)  # each batch row's tokens (ragged batches: its own)
+    chunk = min(chunk, min(rows))
     gen = torch.Generator(device=device)
     gen.manual_seed(wl.seed + 77)
     q = torch.randn((wl.batch, chunk, wl.num_q_heads, wl.head_dim), generator=gen, device=device).half()
@@ -142,16 +143,16 @@ def prefill_attention_timing(wl, model, device, flush, chunk=1024, reps=3):
         torch.cuda.synchronize(device)
         ts.append(a0.elapsed_time(a1))
     assert cache.status() == 0
-    visible = chunk * (S - chunk) + chunk * (chunk + 1) // 2
-    flops = 4 * wl.head_dim * wl.num_q_heads * wl.batch * visible
+    visible = sum(chunk * (n - chunk) + chunk * (chunk + 1) // 2 for n in rows)
+    flops = 4 * wl.head_dim * wl.num_q_heads * visible
     m = statistics.median(ts)
     peak, kind = tensor_peak()
     tf = flops / (m * 1e-3) / 1e12
     return {"ms": round(m, 3), "chunk": chunk, "context": S, "flops": flops, "tflops": round(tf, 1),
             "frac": round(tf / peak, 4), "peak": peak, "peak_kind": kind + " (bf16_tflops, dense; of " + kind + ")",
             "bound": "tensor",
-            "what": "causal attention of the queries of layer 0's last %d positions over its %d cached tokens "
-                    "(kvq_prefill_attention, fp32 out)" % (chunk, S)}
+            "what": "causal attention of the queries of layer 0's last %d positions of every batch row over the "
+                    "row's cached tokens (%d at most; kvq_prefill_attention, fp32 out)" % (chunk, S)}
 
 
 def gpu_id(device):
@@ -411,7 +412,7 @@ def run_gpu(args, wl, rank, world, device):
     del k0, v0
     torch.cuda.synchronize(device)
 
-    pattn = None if wl.lens else prefill_attention_timing(wl, model, device, flush)
+    pattn = prefill_attention_timing(wl, model, device, flush)
     e2e = run_e2e(args, wl, model, st, device)
     err = e2e_error(wl, model, device)
 

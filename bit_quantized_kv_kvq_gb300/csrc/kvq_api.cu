@@ -740,8 +740,9 @@ kvq_status kvq_prefill_attention(kvq_cache* h, int32_t layer, const void* q, int
   if (len == 0) return fail(KVQ_ERR_INVALID_ARG, "layer %d is empty: attention is undefined", layer);
   if (chunk < 1 || chunk > len)
     return fail(KVQ_ERR_INVALID_ARG, "chunk %d must be in [1, %d] (the tokens cached)", chunk, len);
-  if (!h->seq[layer].empty())
-    return fail(KVQ_ERR_UNSUPPORTED, "prefill attention over a layer with variable lengths is not built");
+  const std::vector<int32_t>& sq = h->seq[layer];
+  for (int32_t x : sq)  // variable lengths: every row's chunk is its own last `chunk` positions
+    if (chunk > x) return fail(KVQ_ERR_INVALID_ARG, "chunk %d exceeds a batch row of %d tokens", chunk, x);
   if ((int64_t)chunk * (num_q_heads / hkv) > ((int64_t)1 << 30))
     return fail(KVQ_ERR_INVALID_ARG, "chunk * query heads per kv-head is too large");
   kvq::PrefillAttnArgs a;
@@ -756,6 +757,10 @@ kvq_status kvq_prefill_attention(kvq_cache* h, int32_t layer, const void* q, int
   a.sink_len = sink_len(h->cfg, len);
   a.kq = k_quant_len(h->cfg, coded_len(h->cfg, len));
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  if (!sq.empty()) {
+    a.varlen = 1;
+    for (int b = 0; b < h->cfg.batch; ++b) a.lens[b] = sq[b];
+  }
   const kvq::LayerDev L = layer_dev(h, layer);
   const cudaError_t e = kvq::launch_prefill_attention(L, a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");

@@ -90,6 +90,8 @@ struct PrefillAttnArgs {
   int sink_len;     // fp16 sink tokens among them
   int kq;           // per-channel keys: coded rows held as codes (the rest are the fp16 residual)
   float scale_log2; // softmax scale * log2(e)
+  int varlen;       // batch row b holds lens[b] tokens (its chunk: its last `chunk` positions)
+  int32_t lens[kMaxVarlenBatch];
 };
 cudaError_t launch_prefill_attention(const LayerDev& L, const PrefillAttnArgs& a, cudaStream_t stream);
 

@@ -245,7 +245,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
   const int G = a.G;
   const int rows_total = a.chunk * G;
   const int R0 = blockIdx.x * kRowsCta;
-  const int first_pos = a.length - a.chunk;  // position of query 0
+  // this batch row's tokens (variable lengths: its own, with its own key blocks; no sinks)
+  const int length = a.varlen ? a.lens[b] : a.length;
+  const int kq = a.varlen ? length / L.k.group * L.k.group : a.kq;
+  const int first_pos = length - a.chunk;  // position of query 0
   const int ut = tid >> 4, uc = 8 * (tid & 15);  // the thread's units: tokens ut + 16 k, channels uc ..
 
   for (int idx = tid; idx < kRowsCta * 16; idx += kThreads) {
@@ -264,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
   // positions of the thread's rows g and g + 8 (rows past the chunk attend
   // the whole cache and are not stored)
   const int Rw = R0 + 16 * warp;
-  auto pos_of = [&](int R) { return R < rows_total ? first_pos + R / G : a.length - 1; };
+  auto pos_of = [&](int R) { return R < rows_total ? first_pos + R / G : length - 1; };
   const int pos0 = pos_of(Rw + g), pos1 = pos_of(Rw + g + 8);
   const int warp_pos_max = Rw < rows_total ? pos_of(min(Rw + 15, rows_total - 1)) : -1;  // -1: no rows
   const int last_R = min(R0 + kRowsCta, rows_total) - 1;
@@ -276,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
     for (int k = 0; k < 4; ++k) {
       const int t = ut + 16 * k;
       float x[8];
-      dequant8<true>(L, n, t0 + t, uc, a.length, a.sink_len, a.kq, cbt, x);
+      dequant8<true>(L, n, t0 + t, uc, length, a.sink_len, kq, cbt, x);
       uint4 lo;
       const uint4 hi = split8(x, lo);
       *reinterpret_cast<uint4*>(tb(buf, 0) + t * kLd + uc) = hi;
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
     for (int k = 0; k < 4; ++k) {
       const int t = ut + 16 * k;
       float x[8];
-      dequant8<false>(L, n, t0 + t, uc, a.length, a.sink_len, a.kq, cbt, x);
+      dequant8<false>(L, n, t0 + t, uc, length, a.sink_len, kq, cbt, x);
       uint4 lo;
       const uint4 hi = split8(x, lo);
       *reinterpret_cast<uint4*>(tb(buf, 2) + t * kLd + uc) = hi;
@@ -347,11 +350,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
     __syncthreads();
     const int tn = t0 + kTT;
     const bool more = tile + 1 < n_tiles;
-    const bool nfast = more && fast_tile(L, tn, a.length, a.sink_len, a.kq);
+    const bool nfast = more && fast_tile(L, tn, length, a.sink_len, kq);
     if (nfast)
       load_raw(tn, raw);  // in flight during the products
     else if (more)
-      prefetch_tile(L, n, tn, a.length, a.sink_len, tid);
+      prefetch_tile(L, n, tn, length, a.sink_len, tid);
 
     if (t0 <= warp_pos_max) {  // some token of the tile is visible to the warp's rows
       const __half* khi = tb(buf, 0);

@@ -299,9 +299,11 @@ KVQ_API kvq_status kvq_decode_step(kvq_cache* cache, const void* const* q, const
  * cache is served. No workspace; one launch, one CTA per 128 (position,
  * head) rows of a stream. q and out must be 16-byte aligned; the cache's
  * device must be current.
+ * With variable lengths (kvq_prefill_quantize_varlen) each batch row's
+ * chunk is its own last `chunk` positions.
  * Errors: KVQ_ERR_INVALID_ARG for an empty layer, chunk outside
- * [1, length], NULL or misaligned pointers or a bad out_dtype;
- * KVQ_ERR_UNSUPPORTED for a layer with variable lengths. */
+ * [1, length] (or above a batch row's length), NULL or misaligned pointers
+ * or a bad out_dtype. */
 KVQ_API kvq_status kvq_prefill_attention(kvq_cache* cache, int32_t layer, const void* q, int32_t chunk,
                                          int32_t num_q_heads, float softmax_scale, void* out,
                                          int32_t out_dtype, void* stream);

@@ -5,8 +5,8 @@ against one oracle cache per stream built from that stream's tokens alone:
 codes, scales and outliers of each stream's rows bit-exact, attention within
 1e-3, through the GQA tensor-core kernel and the generic kernel, the
 two-stream decode step, per-channel keys whose residual fills and flushes
-a block at each row's own appends, and the refusals (sinks, lengths out of
-range, prefill attention over ragged rows)."""
+a block at each row's own appends, prefill attention over ragged rows, and
+the refusals (sinks, lengths out of range)."""
 import math
 from dataclasses import replace
 
@@ -139,8 +139,8 @@ def test_uniform_prefill_ends_variable_lengths():
     k, v = LayerSource(wl, 0, device="cpu").kv(64)
     cache = K.make_gpu_cache(wl, 80)
     cache.prefill_varlen(0, k.cuda(), v.cuda(), [3, 64, 9, 10])
-    with pytest.raises(kvq.KVQError):  # prefill attention over ragged rows is not built
-        cache.prefill_attention(0, torch.zeros((4, 2, 8, 128), dtype=torch.float16, device="cuda"), 1.0)
+    with pytest.raises(kvq.KVQError):  # a chunk longer than the shortest row
+        cache.prefill_attention(0, torch.zeros((4, 4, 8, 128), dtype=torch.float16, device="cuda"), 1.0)
     cache.prefill(0, k.cuda(), v.cuda())
     assert cache.seq_lengths(0) == [64, 64, 64, 64]
 
@@ -157,4 +157,30 @@ def test_varlen_refusals():
     sinks = K.make_gpu_cache(tok, 32, sink_tokens=2)
     with pytest.raises(kvq.KVQError):
         sinks.prefill_varlen(0, k.cuda(), v.cuda(), [4, 16])             # with sink tokens
+    assert cache.status() == 0
+
+
+@pytest.mark.parametrize("case", [("q8_0 int8 g4", W.TINY_Q8, 4, [37, 200, 20, 130]),
+                                  ("per-channel k4v8 g4", W.LLAMA8B_FULL, 4, [62, 200, 20, 127]),
+                                  ("per-channel k3v3 g8", W.LLAMA70B_32K, 8, [129, 200, 20, 140])],
+                         ids=lambda c: c[0])
+def test_prefill_attention_over_ragged_rows(case):
+    """Each batch row's chunk is its own last positions: the queries of row
+    b attend row b's tokens causally (one oracle cache per stream)."""
+    name, wl0, g, lens = case
+    wl = replace(wl0, num_layers=1, batch=len(lens), num_kv_heads=2, num_q_heads=2 * g, seq_len=max(lens))
+    H, chunk = wl.num_kv_heads, 19
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(wl.seq_len)
+    cache = K.make_gpu_cache(wl, wl.seq_len + 1)
+    cache.prefill_varlen(0, k.cuda(), v.cuda(), lens)
+    q = torch.randn((wl.batch, chunk, wl.num_q_heads, 128), generator=torch.Generator().manual_seed(9)).half()
+    o = cache.prefill_attention(0, q.cuda(), 1.0 / math.sqrt(128)).cpu().double().numpy()
+    for n in range(wl.batch * H):
+        b, h = divmod(n, H)
+        oc = O.OracleCache(K.spec_of(wl), 1)
+        oc.prefill(k[b, h, :lens[b]].numpy()[None], v[b, h, :lens[b]].numpy()[None])
+        ref = oc.prefill_attention(q[b, :, h * g:(h + 1) * g].double().numpy()[None], 1.0 / math.sqrt(128))
+        K.assert_attention_close(o[b, :, h * g:(h + 1) * g].reshape(-1, 128), ref[0].reshape(-1, 128),
+                                 where="%s stream %d" % (name, n))
     assert cache.status() == 0
