@@ -212,10 +212,14 @@ __device__ __forceinline__ uint4 split8(const float (&x)[8], uint4& lo) {
   return hi;
 }
 
-// A tile whose 64 tokens are all coded rows held as codes, without
-// outliers, in one key block: its packed data can be loaded ahead.
+// A tile whose 64 tokens are all coded rows held as codes, with at most
+// kMaxFastOutliers outliers per row (OUTL) or none, in one key block: its
+// packed data can be loaded ahead.
+constexpr int kMaxFastOutliers = 2;
+
+template <bool OUTL>
 __device__ __forceinline__ bool fast_tile(const LayerDev& L, int t0, int length, int sink_len, int kq) {
-  if (L.outliers > 0 || t0 < sink_len || t0 + kTT > length) return false;
+  if ((OUTL ? L.outliers > kMaxFastOutliers : L.outliers > 0) || t0 < sink_len || t0 + kTT > length) return false;
   if (L.k.mode == KVQ_ASYM_PER_CHANNEL) {
     const int r0 = t0 - sink_len, r1 = r0 + kTT - 1;
     if (r1 >= kq || r0 / L.k.group != r1 / L.k.group) return false;
@@ -225,12 +229,43 @@ __device__ __forceinline__ bool fast_tile(const LayerDev& L, int t0, int length,
 
 // The thread's packed data of a fast tile: four (token, 8-channel) units of
 // K and of V (tokens (tid >> 4) + 16 k, channels 8 (tid & 15) ..).
+template <bool OUTL>
 struct Raw {
   uint32_t kw[4][2], vw[4][2];  // code words
   uint32_t km[4], vm[4];        // per-token scale words
   uint32_t kch[8];              // per-channel key (s, z) of the eight channels (one block)
+  // outliers of each unit's row: columns and fp16 values, two per word
+  uint32_t kc[OUTL ? 4 : 1], kv[OUTL ? 4 : 1], vc[OUTL ? 4 : 1], vv[OUTL ? 4 : 1];
 };
 
+// Outlier slots of a unit (channels c0 .. c0 + 7) from its row's packed
+// columns and values (at most two per row).
+__device__ __forceinline__ void apply_outliers(float (&x)[8], uint32_t cols, uint32_t vals, int kout, int c0) {
+#pragma unroll
+  for (int e = 0; e < kMaxFastOutliers; ++e) {
+    if (e >= kout) break;
+    const int cc = (int)((cols >> (16 * e)) & (kHeadDim - 1)) - c0;
+    const float v = __half2float(__ushort_as_half((unsigned short)(vals >> (16 * e))));
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (j == cc) x[j] = v;
+  }
+}
+
+// Packed outlier columns and values (two per word) of coded row r.
+__device__ __forceinline__ void row_outliers(const TensorDev& T, int n, int r, int kout, uint32_t& cols,
+                                             uint32_t& vals) {
+  const int64_t e0 = (int64_t)n * T.out_sstride + (int64_t)r * kout;
+  if (kout == 2) {  // e0 is even: four-byte aligned pairs
+    cols = __ldg(reinterpret_cast<const uint32_t*>(T.col + e0));
+    vals = __ldg(reinterpret_cast<const uint32_t*>(T.val + e0));
+  } else {
+    cols = __ldg(T.col + e0);
+    vals = __half_as_ushort(__ldg(T.val + e0));
+  }
+}
+
+template <bool OUTL>
 __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDev L, const PrefillAttnArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   __half* qs = reinterpret_cast<__half*>(smem);   // [128][kLd]
@@ -300,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
   const uint32_t* vcodes = L.v.codes + (int64_t)n * L.v.codes_sstride;
   const unsigned char* kmeta = L.k.meta + (int64_t)n * L.k.meta_sstride;
   const unsigned char* vmeta = L.v.meta + (int64_t)n * L.v.meta_sstride;
-  auto load_raw = [&](int t0, Raw& w) {
+  auto load_raw = [&](int t0, Raw<OUTL>& w) {
     const int r0 = t0 - a.sink_len;
     if (L.k.mode == KVQ_ASYM_PER_CHANNEL) channel_meta(kmeta, r0 / L.k.group, uc, w.kch);
 #pragma unroll
@@ -310,9 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
       load_words(vcodes + (int64_t)r * L.v.words, L.v.bits, uc, w.vw[k]);
       w.km[k] = L.k.mode == KVQ_ASYM_PER_CHANNEL ? 0u : token_meta(L.k, kmeta, r, uc);
       w.vm[k] = token_meta(L.v, vmeta, r, uc);
+      if (OUTL) {
+        row_outliers(L.k, n, r, L.outliers, w.kc[k], w.kv[k]);
+        row_outliers(L.v, n, r, L.outliers, w.vc[k], w.vv[k]);
+      }
     }
   };
-  auto convert_raw = [&](const Raw& w, int buf) {
+  auto convert_raw = [&](const Raw<OUTL>& w, int buf) {
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const int t = ut + 16 * k;
@@ -321,11 +360,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
       uint4 lo, hi;
       extract8(w.kw[k], L.k.bits, uc, c);
       decode8(L.k.mode, c, w.km[k], w.kch, cbt, x);
+      if (OUTL) apply_outliers(x, w.kc[k], w.kv[k], L.outliers, uc);
       hi = split8(x, lo);
       *reinterpret_cast<uint4*>(tb(buf, 0) + t * kLd + uc) = hi;
       *reinterpret_cast<uint4*>(tb(buf, 1) + t * kLd + uc) = lo;
       extract8(w.vw[k], L.v.bits, uc, c);
       decode8(L.v.mode, c, w.vm[k], w.kch, cbt, x);  // per-token values: the channel words are unused
+      if (OUTL) apply_outliers(x, w.vc[k], w.vv[k], L.outliers, uc);
       hi = split8(x, lo);
       *reinterpret_cast<uint4*>(tb(buf, 2) + t * kLd + uc) = hi;
       *reinterpret_cast<uint4*>(tb(buf, 3) + t * kLd + uc) = lo;
@@ -343,14 +384,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.0f, l1 = 0.0f;
   const uint32_t qbase = smem_u32(qs + (16 * warp + (lane & 15)) * kLd + 8 * (lane >> 4));
 
-  Raw raw;
+  Raw<OUTL> raw;
   for (int tile = 0; tile < n_tiles; ++tile) {
     const int t0 = tile * kTT, buf = tile & 1;
     // buffer buf holds this tile; every warp is done with the other one
     __syncthreads();
     const int tn = t0 + kTT;
     const bool more = tile + 1 < n_tiles;
-    const bool nfast = more && fast_tile(L, tn, length, a.sink_len, kq);
+    const bool nfast = more && fast_tile<OUTL>(L, tn, length, a.sink_len, kq);
     if (nfast)
       load_raw(tn, raw);  // in flight during the products
     else if (more)
@@ -491,18 +532,26 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
 }  // namespace
 }  // namespace pa
 
-cudaError_t launch_prefill_attention(const LayerDev& L, const PrefillAttnArgs& a, cudaStream_t st) {
+namespace {
+template <bool OUTL>
+cudaError_t launch_pa(const LayerDev& L, const PrefillAttnArgs& a, cudaStream_t st) {
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(pa::prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)pa::kSmemBytes);
+    const cudaError_t e = cudaFuncSetAttribute(pa::prefill_attn_kernel<OUTL>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pa::kSmemBytes);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int rows = a.chunk * a.G;
   const dim3 grid((rows + pa::kRowsCta - 1) / pa::kRowsCta, L.n_streams);
-  pa::prefill_attn_kernel<<<grid, pa::kThreads, pa::kSmemBytes, st>>>(L, a);
+  pa::prefill_attn_kernel<OUTL><<<grid, pa::kThreads, pa::kSmemBytes, st>>>(L, a);
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_prefill_attention(const LayerDev& L, const PrefillAttnArgs& a, cudaStream_t st) {
+  // rows with a few outliers keep the pipelined path in their own instance
+  return L.outliers > 0 && L.outliers <= pa::kMaxFastOutliers ? launch_pa<true>(L, a, st) : launch_pa<false>(L, a, st);
 }
 
 }  // namespace kvq
