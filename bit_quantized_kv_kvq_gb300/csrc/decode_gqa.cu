@@ -19,10 +19,13 @@ bool decode_gqa_supported(const LayerDev& L, int gqa) {
 
 cudaError_t launch_decode_gqa(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
   const int kb = L.k.bits, vb = L.v.bits, km = L.k.mode;
+  const bool g32 = L.k.group == 32 && L.v.group == 32;  // the q8_0 layout: constant groups of 32
   if (km == KVQ_SYM_PER_TOKEN)
-    return gqa::launch_t<8, KVQ_SYM_PER_TOKEN, 8, KVQ_SYM_PER_TOKEN>(L, a, st);
+    return g32 ? gqa::launch_t<8, KVQ_SYM_PER_TOKEN, 8, KVQ_SYM_PER_TOKEN, 32>(L, a, st)
+               : gqa::launch_t<8, KVQ_SYM_PER_TOKEN, 8, KVQ_SYM_PER_TOKEN>(L, a, st);
   if (km == KVQ_CODEBOOK_PER_TOKEN)
-    return gqa::launch_t<4, KVQ_CODEBOOK_PER_TOKEN, 4, KVQ_CODEBOOK_PER_TOKEN>(L, a, st);
+    return g32 ? gqa::launch_t<4, KVQ_CODEBOOK_PER_TOKEN, 4, KVQ_CODEBOOK_PER_TOKEN, 32>(L, a, st)
+               : gqa::launch_t<4, KVQ_CODEBOOK_PER_TOKEN, 4, KVQ_CODEBOOK_PER_TOKEN>(L, a, st);
 #define KVQ_GQA(KB_, KM_)                                                          \
   if (kb == KB_ && km == KM_) {                                                    \
     if (vb == 4) return gqa::launch_t<KB_, KM_, 4, KVQ_ASYM_PER_TOKEN>(L, a, st);  \

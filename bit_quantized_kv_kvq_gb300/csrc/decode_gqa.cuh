@@ -132,7 +132,10 @@ __device__ __forceinline__ int key_channel(int kc, int t4, int which, int gp) {
   }
 }
 
-template <int KB, int KMODE, int VB, int VMODE>
+// FG: 0, or the group size of per-token keys and of values when both are
+// fixed at compile time (then every per-group loop unrolls with constant
+// group indices).
+template <int KB, int KMODE, int VB, int VMODE, int FG>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_gqa_kernel(LayerDev L, DecodeArgs a) {
   using C = Cfg<KB, KMODE, VB, VMODE>;
@@ -160,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   const int per_warp = (ntiles + kWarps - 1) / kWarps;
   const int w_first = min(warp * per_warp, ntiles);
   const int w_count = min(per_warp, ntiles - w_first);
-  const int Gk = L.k.group, Gv = L.v.group;
+  const int Gk = FG ? FG : L.k.group, Gv = FG ? FG : L.v.group;
   const int kgpr = C::KCH ? 1 : kHeadDim / Gk;
   const int vgpr = kHeadDim / Gv;
   const int gp = C::KCH ? kHeadDim : Gk;  // key group that chunks must not straddle
@@ -711,22 +714,22 @@ __global__ void __launch_bounds__(kThreads, 3)
   if (a.splits > 1) merge_splits_if_last<kWarps>(L.counters + n, a, b * a.num_q_heads + hq0, G);
 }
 
-template <int KB, int KMODE, int VB, int VMODE>
+template <int KB, int KMODE, int VB, int VMODE, int FG = 0>
 cudaError_t launch_t(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<KB, KMODE, VB, VMODE>;
   const size_t sm = C::smem_bytes();
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_gqa_kernel<KB, KMODE, VB, VMODE>,
+    cudaError_t e = cudaFuncSetAttribute(decode_gqa_kernel<KB, KMODE, VB, VMODE, FG>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   if (a.occupancy_out)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        a.occupancy_out, decode_gqa_kernel<KB, KMODE, VB, VMODE>, kThreads, sm);
+        a.occupancy_out, decode_gqa_kernel<KB, KMODE, VB, VMODE, FG>, kThreads, sm);
   dim3 grid(a.splits, L.n_streams);
-  decode_gqa_kernel<KB, KMODE, VB, VMODE><<<grid, kThreads, sm, st>>>(L, a);
+  decode_gqa_kernel<KB, KMODE, VB, VMODE, FG><<<grid, kThreads, sm, st>>>(L, a);
   return cudaGetLastError();
 }
 
