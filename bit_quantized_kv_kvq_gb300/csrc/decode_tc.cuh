@@ -110,7 +110,10 @@ struct Cfg {
   }
 };
 
-template <int KB, int VB, int VG, int NT, bool OUTL>
+// GF: 0, or the query heads per kv-head fixed at compile time (1, or every
+// head slot: 4 NT), which removes the per-head guards and the run-time
+// choice of the one-head path.
+template <int KB, int VB, int VG, int NT, bool OUTL, int GF>
 __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
     decode_tc_kernel(LayerDev L, DecodeArgs a) {
   using C = Cfg<KB, VB, VG, NT, OUTL>;
@@ -122,7 +125,7 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
   const int split = blockIdx.x, n = blockIdx.y;
   const int b = n / L.num_kv_heads;
   const int kvh = n - b * L.num_kv_heads;
-  const int G = a.gqa;  // query heads of this kv-head (<= 4 NT)
+  const int G = GF ? GF : a.gqa;  // query heads of this kv-head (<= 4 NT)
   const int hq0 = kvh * G;
 
   constexpr int H = C::H;
@@ -962,11 +965,11 @@ __global__ void __launch_bounds__(kThreads, NT == 1 ? 4 : 3)
   if (a.splits > 1) merge_splits_if_last<kWarps>(L.counters + n, a, b * a.num_q_heads + hq0, G);
 }
 
-template <int KB, int VB, int VG, int NT, bool OUTL>
+template <int KB, int VB, int VG, int NT, bool OUTL, int GF = 0>
 cudaError_t launch_t(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<KB, VB, VG, NT, OUTL>;
   const size_t sm = C::smem_bytes(OUTL ? L.outliers : 0, NT == 1 && a.gqa == 1);
-  auto kern = decode_tc_kernel<KB, VB, VG, NT, OUTL>;
+  auto kern = decode_tc_kernel<KB, VB, VG, NT, OUTL, GF>;
   static bool attr_set = false;
   if (!attr_set) {  // room for the most outliers a row may hold
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
