@@ -398,6 +398,30 @@ def test_tensor_core_decode_outlier_counts(kout, gqa, vg):
     _run_case(wl, appends=2, check_every=1)
 
 
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 0])
+@pytest.mark.parametrize("seq", [335, 1000])
+@pytest.mark.parametrize("vg", [64, 128])
+def test_one_head_outlier_split_counts(splits, seq, vg):
+    """One query head, eight outliers per row (half of each lane's value
+    corrections go through the shared atomics): the same attention for every
+    split layout, the last split ragged and the key residual non-empty."""
+    wl = replace(W.DENSE_SPARSE_128K, batch=1, num_q_heads=2, num_kv_heads=2, seq_len=seq,
+                 outliers_per_row=8, v_group=vg)
+    src = LayerSource(wl, 0, device="cpu")
+    k, v = src.kv(wl.seq_len)
+    q, _, _ = src.step(3)
+    cache = K.make_gpu_cache(wl, wl.seq_len)
+    cache.prefill(0, k.cuda(), v.cuda())
+    oc = O.OracleCache(K.spec_of(wl), wl.batch * wl.num_kv_heads)
+    oc.prefill(K.streams_of(k, wl), K.streams_of(v, wl))
+    ref = oc.decode(K.q_streams(q, wl), 0.088)
+    cache.set_decode_splits(splits)
+    for _ in range(3):  # repeated: the atomics' order varies between launches
+        o = cache.decode(0, q.cuda(), 0.088).cpu().double().reshape(ref.shape).numpy()
+        K.assert_attention_close(o, ref, where="splits %d" % splits)
+    assert cache.status() == 0
+
+
 @pytest.mark.parametrize("outliers", [0, 2])
 def test_one_head_late_max_rescale(outliers):
     """One query head, one split: keys of every other 32-token tile scaled by
