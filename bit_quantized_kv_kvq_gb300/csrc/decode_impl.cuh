@@ -412,12 +412,10 @@ template <int KB, int KMODE, int VB, int VMODE, int G>
 cudaError_t launch_decode_t(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
   using C = DecodeCfg<KB, KMODE, VB, VMODE, G>;
   const size_t sm = C::smem_bytes();
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<KB, KMODE, VB, VMODE, G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  static SmemAttr attr;
+  {
+    const cudaError_t e = attr.ensure(decode_split_kernel<KB, KMODE, VB, VMODE, G>, sm);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   if (a.occupancy_out)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(

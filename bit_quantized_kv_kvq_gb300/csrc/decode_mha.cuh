@@ -481,12 +481,10 @@ template <int KB, int KMODE, int VB, int VMODE, bool OUTL>
 cudaError_t launch_t(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<KB, KMODE, VB, VMODE, OUTL>;
   const size_t sm = C::smem_bytes();
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_mha_kernel<KB, KMODE, VB, VMODE, OUTL>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
+  static SmemAttr attr;
+  {
+    const cudaError_t e = attr.ensure(decode_mha_kernel<KB, KMODE, VB, VMODE, OUTL>, sm);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   if (a.occupancy_out)
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(

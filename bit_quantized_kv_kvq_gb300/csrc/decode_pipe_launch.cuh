@@ -75,11 +75,10 @@ cudaError_t launch_t(const LayerDev& L, Args a, cudaStream_t st) {
     if (e != cudaSuccess) return e;
   }
   auto kern = decode_pipe_kernel<KB, VB, VG, OUTL>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemMax);
+  static SmemAttr attr;
+  {
+    const cudaError_t e = attr.ensure(kern, kSmemMax);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   kern<<<a.P, kThreads, smem, st>>>(maps, L, a);
   return cudaGetLastError();

@@ -970,12 +970,10 @@ cudaError_t launch_t(const LayerDev& L, const DecodeArgs& a, cudaStream_t st) {
   using C = Cfg<KB, VB, VG, NT, OUTL>;
   const size_t sm = C::smem_bytes(OUTL ? L.outliers : 0, NT == 1 && a.gqa == 1);
   auto kern = decode_tc_kernel<KB, VB, VG, NT, OUTL, GF>;
-  static bool attr_set = false;
-  if (!attr_set) {  // room for the most outliers a row may hold
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::smem_bytes(OUTL ? kMaxOutliers : 0));
+  static SmemAttr attr;
+  {  // room for the most outliers a row may hold
+    const cudaError_t e = attr.ensure(kern, C::smem_bytes(OUTL ? kMaxOutliers : 0));
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   if (a.occupancy_out) return cudaOccupancyMaxActiveBlocksPerMultiprocessor(a.occupancy_out, kern, kThreads, sm);
   dim3 grid(a.splits, L.n_streams);

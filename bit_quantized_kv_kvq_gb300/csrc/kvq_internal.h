@@ -3,6 +3,7 @@
 
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <atomic>
 #include <cstdint>
 
 #include "kvq.h"
@@ -12,6 +13,28 @@ namespace kvq {
 constexpr int kHeadDim = 128;   // channels per (token, head) row
 constexpr int kTile = 64;       // decode tile (tokens) and capacity granularity
 constexpr int kMaxOutliers = 8; // per (token, head) row
+
+// The dynamic shared memory a kernel may take beyond the default, set the
+// first time the kernel launches on each device: the attribute belongs to the
+// kernel's image in one device's context, so every device needs its own call.
+// One instance per kernel; devices past ordinal 63 set it on every launch.
+class SmemAttr {
+ public:
+  template <typename K>
+  cudaError_t ensure(K* kern, size_t bytes) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done_.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess && bit) done_.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+  }
+
+ private:
+  std::atomic<unsigned long long> done_{0};
+};
 
 // Device status bits (see kvq_cache_status).
 constexpr uint32_t kStatusTimeout = 1u << 0;

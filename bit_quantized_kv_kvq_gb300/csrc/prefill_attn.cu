@@ -535,12 +535,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_attn_kernel(const LayerDe
 namespace {
 template <bool OUTL>
 cudaError_t launch_pa(const LayerDev& L, const PrefillAttnArgs& a, cudaStream_t st) {
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(pa::prefill_attn_kernel<OUTL>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)pa::kSmemBytes);
+  static SmemAttr attr;
+  {
+    const cudaError_t e = attr.ensure(pa::prefill_attn_kernel<OUTL>, pa::kSmemBytes);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const int rows = a.chunk * a.G;
   const dim3 grid((rows + pa::kRowsCta - 1) / pa::kRowsCta, L.n_streams);

@@ -1026,12 +1026,14 @@ cudaError_t launch_fast_t(const LayerDev& L, const __half* k, const __half* v, i
                           cudaStream_t st) {
   using G = Geo<KB, KMODE, TB, VB, OUTL>;
   auto kern = prefill_fast_kernel<KB, KMODE, TB, VB, VSYM, OUTL>;
+  static SmemAttr attr;
   static int occ = 0;
-  if (occ == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)G::kBytes);
+  {
+    const cudaError_t e = attr.ensure(kern, G::kBytes);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * G::kW, G::kBytes);
+  }
+  if (occ == 0) {
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * G::kW, G::kBytes);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
   }

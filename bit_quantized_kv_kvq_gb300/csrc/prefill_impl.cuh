@@ -887,12 +887,14 @@ cudaError_t launch_prefill_t(const LayerDev& L, const __half* k, const __half* v
                              cudaStream_t st) {
   using SM = PrefillSmem<KB, KMODE, KR, VB, VSYM>;
   auto kern = prefill_kernel<KB, KMODE, KR, VB, VSYM>;
+  static SmemAttr attr;
   static int occ = 0;
-  if (occ == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SM::bytes);
+  {
+    const cudaError_t e = attr.ensure(kern, SM::bytes);
     if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, SM::bytes);
+  }
+  if (occ == 0) {
+    const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, SM::bytes);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
   }
