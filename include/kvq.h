@@ -31,11 +31,13 @@
  *    the work enqueued on it has finished. Device pointers must be 16-byte
  *    aligned; the cache buffer 256-byte aligned.
  *  - fp16 means IEEE binary16. Layouts are C order (last index fastest).
- *  - One cache serves num_layers layers; lengths are uniform over the
- *    batch. head_dim must be 128.
+ *  - One cache serves num_layers layers; a layer's lengths are uniform over
+ *    the batch unless kvq_prefill_quantize_varlen gave each batch row its
+ *    own. head_dim must be 128.
  *  - Calls that enqueue work (prefill, append, decode, status) need the
  *    device that holds the cache buffer to be current; otherwise they
- *    return KVQ_ERR_INVALID_ARG.
+ *    return KVQ_ERR_INVALID_ARG. Caches on several devices may be used from
+ *    one process (kernel attributes are set per device).
  */
 #ifndef KVQ_H
 #define KVQ_H
