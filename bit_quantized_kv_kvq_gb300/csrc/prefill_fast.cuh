@@ -1027,15 +1027,17 @@ cudaError_t launch_fast_t(const LayerDev& L, const __half* k, const __half* v, i
   using G = Geo<KB, KMODE, TB, VB, OUTL>;
   auto kern = prefill_fast_kernel<KB, KMODE, TB, VB, VSYM, OUTL>;
   static SmemAttr attr;
-  static int occ = 0;
+  static std::atomic<int> occ_cached{0};  // resident CTAs per SM, computed once
   {
     const cudaError_t e = attr.ensure(kern, G::kBytes);
     if (e != cudaSuccess) return e;
   }
+  int occ = occ_cached.load(std::memory_order_relaxed);
   if (occ == 0) {
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, 32 * G::kW, G::kBytes);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
+    occ_cached.store(occ, std::memory_order_relaxed);
   }
   Args a;
   a.k = L.k;

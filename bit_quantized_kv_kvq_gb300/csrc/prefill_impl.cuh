@@ -888,15 +888,17 @@ cudaError_t launch_prefill_t(const LayerDev& L, const __half* k, const __half* v
   using SM = PrefillSmem<KB, KMODE, KR, VB, VSYM>;
   auto kern = prefill_kernel<KB, KMODE, KR, VB, VSYM>;
   static SmemAttr attr;
-  static int occ = 0;
+  static std::atomic<int> occ_cached{0};  // resident CTAs per SM, computed once
   {
     const cudaError_t e = attr.ensure(kern, SM::bytes);
     if (e != cudaSuccess) return e;
   }
+  int occ = occ_cached.load(std::memory_order_relaxed);
   if (occ == 0) {
     const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, SM::bytes);
     if (e != cudaSuccess) return e;
     if (occ < 1) occ = 1;
+    occ_cached.store(occ, std::memory_order_relaxed);
   }
   PrefillArgs a;
   a.k = L.k;
